@@ -1,0 +1,421 @@
+"""Benchmark of the online-softmax attention library on GB300.
+
+One step = one attention forward (attn_fwd) over the prefill workload B=4, H=32,
+N=4096, D=128, bf16, causal, inputs resident in HBM (Q, K and V are 402 MB together,
+larger than L2).  Rank 0 prints one JSON line:
+  value     whole-job attention TFLOP/s (algorithmic causal FLOPs 4*B*H*D*N(N+1)/2)
+  e2e       the same metric through the public API with pinned host buffers and the
+            host<->device copies inside the timed region
+  roofline  the attention kernel against the measured dense BF16 peak
+  combine   split-K LSE combine GB/s on 4096x32 row-heads, depth 128, P in {2,8,16,32,37}
+  decode_splitk  split-K decode (64 x 32 heads, 32768 keys) + combine, GB/s
+  cpu_baseline   the FP64 oracle on the host cores, on a bounded sample
+With --impl reference the FP64 oracle itself is timed (host cores) on samples of
+the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s & % BF16 peak (N=4096,D=128); split-K combine HBM GB/s"
+B, H, N, D = 4, 32, 4096, 128
+CAUSAL = True
+SEED = 3
+FLOPS = 4.0 * B * H * D * N * (N + 1) / 2  # algorithmic causal FLOPs per step
+WORKLOAD = "prefill attention forward B=4 H=32 N=4096 D=128 bf16 causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_prefill_b4h32n4096d128.md")
+KERNEL_SOURCES = ["online_softmax_gb300/csrc/attn_fwd.cuh", "online_softmax_gb300/csrc/ptx.cuh",
+                  "online_softmax_gb300/csrc/tmem_regs.cuh"]
+
+
+# ---------------------------------------------------------------- host-side helpers
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over the process group (identity when world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; otherwise None."""
+    if not os.path.exists(PROFILE):
+        return None
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle baseline
+def oracle_sample(budget_s: float, max_heads: int = B * H):
+    """Time the FP64 oracle on whole heads of the prefill workload until `budget_s` of
+    CPU work has run.  Returns (TFLOP/s, seconds, heads)."""
+    import numpy as np
+    import oracle
+    import synth
+    from tests import helpers as Hl
+    done, t_total = 0, 0.0
+    while done < max_heads and (t_total < budget_s or done == 0):
+        bh = done
+        qh = Hl.head_slice(SEED, synth.STREAM_Q, bh, N, D, "bf16")
+        kh = Hl.head_slice(SEED, synth.STREAM_K, bh, N, D, "bf16")
+        vh = Hl.head_slice(SEED, synth.STREAM_V, bh, N, D, "bf16")
+        t0 = time.perf_counter()
+        oracle.attention(qh, kh, vh, 1.0 / math.sqrt(D), CAUSAL)
+        t_total += time.perf_counter() - t0
+        done += 1
+        del qh, kh, vh
+        np.empty(0)
+    flops = 4.0 * D * N * (N + 1) / 2 * done
+    return flops / t_total / 1e12, t_total, done
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    # one step = the oracle on one whole head of the workload (bounded CPU work)
+    for _ in range(args.warmup):
+        oracle_sample(0.0, max_heads=1)
+    times = []
+    for _ in range(args.steps):
+        _, t, _ = oracle_sample(0.0, max_heads=1)
+        times.append(t)
+    per_step = sum(times) / len(times)
+    flops_step = 4.0 * D * N * (N + 1) / 2
+    value = flops_step / per_step / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
+                   "sample": "one head (4096 queries x 4096 keys) per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one whole head of the workload per step, FP64 numpy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU measurements
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="headline only (no combine/decode/e2e)")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import online_softmax_gb300 as ops
+    import synth
+    import synth.cuda as sc
+
+    stream = torch.cuda.current_stream()
+    pk, pk_kind = peaks()
+
+    # ---- inputs of the prefill workload, resident in HBM
+    def rand(stream_id):
+        t = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+        return sc.fill_normal(t, SEED, stream_id, "bf16")
+    q, k, v = rand(synth.STREAM_Q), rand(synth.STREAM_K), rand(synth.STREAM_V)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def step():
+        ops.attn_fwd(q, k, v, o, lse, causal=CAUSAL)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world, dev)
+    assert ops.device_error() == 0
+    value = FLOPS * args.steps * world / (ms_max / 1e3) / 1e12
+    per_launch_s = ms / 1e3 / args.steps
+    achieved = FLOPS / per_launch_s / 1e12
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
+                   "flops_per_step": FLOPS, "l2": "inputs larger than L2 (Q, K, V = 402 MB per step)",
+                   "parallelism": "replicas" if world == 1 else f"replicas x{world} (independent batches)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{pk_kind} (dense bf16 burst)", "kernel": "attn_fwd_kernel<128,128,bf16>"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_extras:
+        line["e2e"] = measure_e2e(torch, ops, q, k, v, args, world, dev)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+        line["combine"] = measure_combine(torch, ops, sc, synth, pk, dev)
+        line["decode_splitk"] = measure_decode(torch, ops, sc, synth, pk, dev)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, secs, heads = oracle_sample(12.0)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{heads} whole heads (4096x4096 causal, D=128) of the workload, "
+                                          f"FP64 numpy oracle, {secs:.1f} s"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(torch, ops, q, k, v, args, world, dev):
+    """Same metric through the public API with pinned host inputs and outputs."""
+    stream = torch.cuda.current_stream()
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+    do = torch.empty_like(q)
+    dl = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ho = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
+    hl = torch.empty(dl.shape, dtype=dl.dtype, pin_memory=True)
+    steps = max(10, min(args.steps, 200))
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ops.attn_fwd(dq, dk, dv, do, dl, causal=CAUSAL)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return {"value": FLOPS * steps * world / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps}
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+def time_launches(torch, fn, iters, flush=None):
+    """Median and mean device time of `fn` over `iters` launches (L2 flushed before each)."""
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    return statistics.median(ts), sum(ts) / len(ts)
+
+
+def measure_combine(torch, ops, sc, synth, pk, dev):
+    rows, heads, depth = 4096, 32, 128
+    RH = rows * heads
+    l2buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out = {"workload": "4096 tokens x 32 heads, depth 128, lse ~ N(10,2), 5% -inf, 0.1% rows all -inf",
+           "unit": "GB/s", "l2": "flushed before every launch (512 MB write)", "results": []}
+    best = None
+    for dt, esz in (("f32", 4), ("bf16", 2)):
+        for P in (2, 8, 16, 32, 37):
+            op = sc.fill_normal(torch.empty((P, RH, depth), dtype=getattr(torch, {"f32": "float32", "bf16": "bfloat16"}[dt]),
+                                            device=dev), 21, synth.STREAM_OPART, dt)
+            lp = sc.fill_lse(torch.empty((P, RH), dtype=torch.float32, device=dev), 21)
+            o = torch.empty((RH, depth), dtype=op.dtype, device=dev)
+            g = torch.empty(RH, dtype=torch.float32, device=dev)
+            fn = lambda: ops.splitk_combine(op, lp, o, g, rows=rows, heads=heads)
+            fn()
+            med, mean = time_launches(torch, fn, 20, flush=lambda: flush_l2(l2buf))
+            nbytes = P * RH * depth * esz + P * RH * 4 + RH * depth * esz + RH * 4
+            gbs = nbytes / med / 1e9
+            r = {"P": P, "dtype": dt, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs,
+                 "frac": gbs / pk["hbm_gbs"]}
+            out["results"].append(r)
+            if best is None or r["frac"] > best["frac"]:
+                best = r
+            del op, lp, o, g
+    assert ops.device_error() == 0
+    del l2buf
+    fr = [r["frac"] for r in out["results"]]
+    out["roofline"] = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
+                       "frac_min": min(fr), "frac_median": statistics.median(fr), "frac_max": max(fr)}
+    return out
+
+
+def measure_decode(torch, ops, sc, synth, pk, dev):
+    Bd, Hd, Nkv, Dd = 64, 32, 32768, 128
+    q = sc.fill_normal(torch.empty((Bd, Hd, 1, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_Q, "bf16")
+    k = sc.fill_normal(torch.empty((Bd, Hd, Nkv, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_K, "bf16")
+    v = sc.fill_normal(torch.empty((Bd, Hd, Nkv, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_V, "bf16")
+    RH = Bd * Hd
+    out = {"workload": "decode: 64 sequences x 1 query, 32 heads, 32768 keys, D=128, bf16; fp32 partials, then combine",
+           "unit": "GB/s", "l2": "K and V (34.4 GB) are far larger than L2", "results": []}
+    for P in (4, 8, 16, 37):
+        op = torch.empty((P, RH, Dd), dtype=torch.float32, device=dev)
+        lp = torch.empty((P, RH), dtype=torch.float32, device=dev)
+        o = torch.empty_like(q)
+        fn = lambda: ops.attn_fwd_splitk(q, k, v, P, op, lp, o, None)
+        fn()
+        med, _ = time_launches(torch, fn, 10)
+        nbytes = 2 * Bd * Hd * Nkv * Dd * 2 + q.numel() * 2 + 2 * (P * RH * Dd * 4 + P * RH * 4) + o.numel() * 2
+        gbs = nbytes / med / 1e9
+        out["results"].append({"P": P, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"]})
+    assert ops.device_error() == 0
+    fr = [r["frac"] for r in out["results"]]
+    out["roofline"] = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "frac_min": min(fr),
+                       "frac_max": max(fr)}
+    del q, k, v
+    return out
+
+
+if __name__ == "__main__":
+    main()

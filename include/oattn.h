@@ -1,0 +1,142 @@
+/*
+ * oattn.h - C ABI of the online-softmax attention library for NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, all asynchronous on the caller's CUDA stream:
+ *
+ *   attn_fwd         single-pass tiled scaled-dot-product attention forward with the
+ *                    online-softmax recurrence ("A3. Tiled attention with online
+ *                    normalization", sections "Keep three quantities for each query row"
+ *                    and "Masks that preserve the recurrence"; "Streaming attention and
+ *                    online state", section "Online statistics").
+ *   attn_fwd_splitk  the same attention with the key axis cut into P partitions; each
+ *                    partition writes its locally normalised output O_p and a base-2
+ *                    log-sum-exp lse_p ("fa4_splitk_combine", workspace layout), then,
+ *                    when an output pointer is given, the partitions are merged.
+ *   splitk_combine   the LSE-weighted merge of P partitions ("fa4_splitk_combine",
+ *                    the per row-head formulas for m*, global_lse, scale_p and O[d]).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named q, k, v, o, lse, o_partial, lse_partial are DEVICE pointers owned by
+ *     the caller; the library never allocates, frees or retains them.  Every tensor is
+ *     dense and row-major (last index contiguous).  16-bit and float32 tensors must start
+ *     on a 16-byte boundary; float LSE arrays on a 4-byte boundary.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is enqueued
+ *     and the call returns without synchronising.  Argument errors are returned before
+ *     anything is launched; a failed launch returns OATTN_ERR_CUDA.
+ *   - Scores are s = scale * q.k.  Causal masking keeps key index <= query index (the
+ *     diagonal included) and requires equal query and key lengths.
+ *   - A query row with no visible key produces output +0 and LSE -inf.
+ *   - Arithmetic: FP32 running max, sum and numerator; exp as ex2.approx of a scaled
+ *     argument; the probabilities are rounded to the input dtype (round to nearest
+ *     even) before the P.V product while the denominator sums the unrounded FP32 values.
+ *   - Every wait inside the kernels is bounded.  A wait that gives up records a code in
+ *     a device status word and the kernel returns early (its outputs are then
+ *     undefined); read and clear that word with oattn_device_error().
+ *   - Not thread-safe across host threads for the first call on a new device (one-time
+ *     set-up); afterwards calls are independent.
+ */
+#ifndef OATTN_H
+#define OATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st*` */
+
+typedef enum {
+  OATTN_OK = 0,
+  OATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad dtype     */
+  OATTN_ERR_UNSUPPORTED = 2, /* valid request outside the compiled instances (e.g. D=96) */
+  OATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a kernel launch failed     */
+  OATTN_ERR_TIMEOUT = 4      /* reported by oattn_device_error(): a bounded wait gave up */
+} oattn_status;
+
+typedef enum { OATTN_F16 = 0, OATTN_BF16 = 1, OATTN_F32 = 2 } oattn_dtype;
+
+/*
+ * attn_fwd - O = softmax(scale * Q K^T [causal mask]) V and the per-row log-sum-exp.
+ *
+ *   q, k, v  [B, H, N, D] dtype (f16 or bf16); o [B, H, N, D] same dtype.
+ *   lse      [B, H, N] float32, natural-log log-sum-exp of the scaled scores of each row
+ *            (M + ln L); may be NULL.
+ *   D in {16, 32, 64, 128}; N >= 0 (N == 0 is a no-op); B, H >= 1; scale finite, > 0.
+ * Returns OATTN_OK, OATTN_ERR_INVALID_ARG or OATTN_ERR_UNSUPPORTED (dtype f32, other D),
+ * or OATTN_ERR_CUDA.
+ */
+oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int N, int D, int causal, float scale,
+                      oattn_dtype dtype, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_bn - attn_fwd with an explicit key-tile width block_n in {32, 64, 128}
+ * ("A3. Tiled attention ...", section "Implement in four stages": BN is exposed as a
+ * tuning choice).  block_n == 0 picks the default (128).  Results differ from attn_fwd
+ * only by floating-point summation order.
+ */
+oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int D, int causal, float scale,
+                         oattn_dtype dtype, int block_n, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_splitk - attention with the key axis split into P partitions.
+ *
+ *   q [B, H, Nq, D]; k, v [B, H, Nkv, D]; dtype f16 or bf16; D in {16, 32, 64, 128}.
+ *   Partition p holds keys [p*C, min((p+1)*C, Nkv)) with
+ *   C = splitk_chunk(Nkv, P) = ceil(ceil(Nkv/P)/128)*128; trailing partitions may be empty.
+ *   o_partial [P, B*H*Nq, D] of partial_dtype (f32, or the input dtype): partition p's
+ *            output normalised by its own sum; row-heads are flattened in (b, h, n)
+ *            order, which for Nq == 1 is the (token, head) order of the combine page.
+ *   lse_partial [P, B*H*Nq] float32, base-2: lse_p = m_p + log2(l_p) with m_p the
+ *            partition's row max of scale*q.k*log2(e).  A (row, partition) with no
+ *            visible key stores O_p = +0 and lse_p = -inf.
+ *   o        NULL: stop after the partials.  Otherwise [B, H, Nq, D] dtype receives the
+ *            merged attention output (splitk_combine over the partials).
+ *   lse      NULL, or [B, H, Nq] float32 natural-log LSE of the merged result (needs o).
+ *   1 <= P <= 256; causal requires Nq == Nkv.
+ * o_partial and lse_partial are scratch owned by the caller and must not overlap q, k, v,
+ * o or lse.
+ */
+oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int Nq, int Nkv, int D, int causal, float scale,
+                             oattn_dtype dtype, int P, void* o_partial, float* lse_partial,
+                             oattn_dtype partial_dtype, struct CUstream_st* stream);
+
+/*
+ * splitk_combine - merge P partitions by their base-2 LSEs ("fa4_splitk_combine").
+ *
+ *   o_partial   [P, rows*heads, depth] of in_dtype (f32, f16 or bf16), each partition
+ *               normalised by its own sum; row-head index rh = row*heads + head.
+ *   lse_partial [P, rows*heads] float32, base 2; -inf marks an empty partition.
+ *   o           [rows*heads, depth] of out_dtype (f32, f16 or bf16).
+ *   lse_out     NULL, or [rows*heads] float32 receiving global_lse (base 2).
+ *   Per row-head: m* = max_p lse_p; global_lse = log2(sum_p 2^(lse_p - m*)) + m*;
+ *   O[d] = sum_p 2^(lse_p - global_lse) * o_partial[p, rh, d].  Partitions whose lse_p is
+ *   -inf contribute nothing; a row-head whose every lse_p is -inf gets O = +0 and
+ *   global_lse = -inf.  o_partial must be finite where lse_p is finite.
+ *   1 <= P <= 256; rows, heads >= 1; depth a power of two with depth*sizeof(in_dtype)
+ *   between 32 and 1024 bytes (f32: 8..256, f16/bf16: 16..512).
+ */
+oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o,
+                            float* lse_out, int P, int rows, int heads, int depth,
+                            oattn_dtype in_dtype, oattn_dtype out_dtype,
+                            struct CUstream_st* stream);
+
+/* Key chunk per partition used by attn_fwd_splitk (host-only, no GPU needed). */
+int splitk_chunk(int Nkv, int P);
+
+/* Human-readable name of a status code (static string). */
+const char* oattn_status_string(oattn_status s);
+
+/*
+ * oattn_device_error - read and clear the device status word of the current device.
+ * Synchronises the current device.  *code receives 0 when no bounded wait gave up
+ * since the last call, else a nonzero site code; returns OATTN_ERR_TIMEOUT in that case,
+ * OATTN_OK otherwise, or OATTN_ERR_CUDA if the device could not be queried.
+ */
+oattn_status oattn_device_error(int* code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OATTN_H */

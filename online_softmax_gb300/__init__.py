@@ -1,0 +1,185 @@
+"""Online-softmax attention for GB300 (sm_103a): Python binding of liboattn.so.
+
+Thin ctypes marshalling over the C ABI in ``include/oattn.h``: every function
+takes torch CUDA tensors, checks shapes, dtypes and contiguity, and passes raw
+device pointers plus the current CUDA stream.  All arithmetic runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and importing the
+package fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "splitk_combine", "splitk_chunk",
+           "device_error", "OattnError", "library_path", "lib"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "_build", "liboattn.so")
+
+OK, INVALID_ARG, UNSUPPORTED, CUDA_ERR, TIMEOUT = 0, 1, 2, 3, 4
+F16, BF16, F32 = 0, 1, 2
+
+
+class OattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lib.oattn_status_string(status).decode()} (status {status})")
+
+
+def _load():
+    if not os.path.exists(library_path):
+        raise ImportError(
+            f"{library_path} is missing: build it with `python -m online_softmax_gb300.build` "
+            "(the package has no fallback path)")
+    L = ctypes.CDLL(library_path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.attn_fwd_bn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    L.attn_fwd_splitk.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i, vp]
+    L.splitk_combine.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
+    L.splitk_chunk.argtypes = [i, i]
+    L.oattn_status_string.argtypes = [i]
+    L.oattn_status_string.restype = ctypes.c_char_p
+    L.oattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "splitk_combine", "splitk_chunk",
+                 "oattn_device_error"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+class _Lazy:
+    """Loads the library on first use, so that building it (``python -m
+    online_softmax_gb300.build``) does not need it to exist yet."""
+    _L = None
+
+    def __getattr__(self, name):
+        if _Lazy._L is None:
+            _Lazy._L = _load()
+        return getattr(_Lazy._L, name)
+
+
+lib = _Lazy()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t == torch.float16:
+        return F16
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(x):
+    return None if x is None else ctypes.c_void_p(x.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(x, name, dtype=None, shape=None):
+    if x is None:
+        return
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and x.dtype != dtype:
+        raise TypeError(f"{name} has dtype {x.dtype}, expected {dtype}")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
+
+
+def _raise(st, what):
+    if st != OK:
+        raise OattnError(st, what)
+
+
+def attn_fwd_bn(q, k, v, o, lse=None, causal=False, scale=None, block_n=0, stream=None):
+    """Attention forward.  q, k, v, o: [B, H, N, D] f16/bf16; lse: [B, H, N] f32 or None."""
+    import torch
+    B, H, N, D = q.shape
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, q.shape)
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, N))
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = lib.attn_fwd_bn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, int(bool(causal)),
+                         scale, _dtype_code(q.dtype), int(block_n), _stream(stream))
+    _raise(st, "attn_fwd_bn")
+    return o, lse
+
+
+def attn_fwd(q, k, v, o, lse=None, causal=False, scale=None, stream=None):
+    """Attention forward with the default key tile (see attn_fwd_bn)."""
+    import torch
+    B, H, N, D = q.shape
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, q.shape)
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, N))
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, int(bool(causal)),
+                      scale, _dtype_code(q.dtype), _stream(stream))
+    _raise(st, "attn_fwd")
+    return o, lse
+
+
+def splitk_chunk(nkv: int, P: int) -> int:
+    """Keys per split-K partition used by attn_fwd_splitk."""
+    return lib.splitk_chunk(int(nkv), int(P))
+
+
+def attn_fwd_splitk(q, k, v, P, o_partial, lse_partial, o=None, lse=None, causal=False,
+                    scale=None, stream=None):
+    """Split-K attention.  q: [B, H, Nq, D]; k, v: [B, H, Nkv, D];
+    o_partial: [P, B*H*Nq, D] f32 or q.dtype; lse_partial: [P, B*H*Nq] f32 (base 2);
+    o: [B, H, Nq, D] q.dtype or None; lse: [B, H, Nq] f32 (natural log) or None."""
+    import torch
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    _check(q, "q"); _check(k, "k", q.dtype, (B, H, Nkv, D)); _check(v, "v", q.dtype, (B, H, Nkv, D))
+    _check(o_partial, "o_partial", None, (P, B * H * Nq, D))
+    _check(lse_partial, "lse_partial", torch.float32, (P, B * H * Nq))
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, Nq))
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = lib.attn_fwd_splitk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nkv, D,
+                             int(bool(causal)), scale, _dtype_code(q.dtype), int(P), _ptr(o_partial),
+                             _ptr(lse_partial), _dtype_code(o_partial.dtype), _stream(stream))
+    _raise(st, "attn_fwd_splitk")
+    return o_partial, lse_partial, o, lse
+
+
+def splitk_combine(o_partial, lse_partial, o, lse_out=None, rows=None, heads=1, stream=None):
+    """LSE-weighted combine.  o_partial: [P, RH, depth]; lse_partial: [P, RH] f32 (base 2);
+    o: [RH, depth] (any shape with RH*depth elements); lse_out: [RH] f32 or None.
+    RH = rows * heads (rows defaults to RH / heads)."""
+    import torch
+    P, RH, depth = o_partial.shape
+    if rows is None:
+        rows = RH // heads
+    if rows * heads != RH:
+        raise ValueError("rows * heads must equal the row-head count")
+    _check(o_partial, "o_partial"); _check(lse_partial, "lse_partial", torch.float32, (P, RH))
+    _check(o, "o")
+    if o.numel() != RH * depth:
+        raise ValueError("o must hold rows*heads*depth elements")
+    _check(lse_out, "lse_out", torch.float32)
+    if lse_out is not None and lse_out.numel() != RH:
+        raise ValueError("lse_out must hold rows*heads elements")
+    st = lib.splitk_combine(_ptr(o_partial), _ptr(lse_partial), _ptr(o), _ptr(lse_out), int(P),
+                            int(rows), int(heads), int(depth), _dtype_code(o_partial.dtype),
+                            _dtype_code(o.dtype), _stream(stream))
+    _raise(st, "splitk_combine")
+    return o, lse_out
+
+
+def device_error() -> int:
+    """Read and clear the device status word (synchronises the device); 0 = no wait gave up."""
+    code = ctypes.c_int(0)
+    st = lib.oattn_device_error(ctypes.byref(code))
+    if st not in (OK, TIMEOUT):
+        raise OattnError(st, "oattn_device_error")
+    return code.value

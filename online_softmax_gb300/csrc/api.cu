@@ -1,0 +1,262 @@
+// C ABI entry points: argument checks, TMA descriptors, dispatch to the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/oattn.h"
+#include "internal.h"
+
+namespace oattn {
+namespace {
+
+// Device status word: a bounded wait that gives up records its site code here.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_setup_mutex;
+
+// Device address of the status word for the current device (looked up once per device).
+unsigned int* status_ptr(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  if (g_status_ptr[dev] == nullptr) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      *err = cudaGetSymbolAddress(&p, g_status_word);
+      if (*err != cudaSuccess) return nullptr;
+      g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+  }
+  return g_status_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D tiled map over a [BH, rows, D] 16-bit tensor; box = (min(D,64) elements, box_rows, 1)
+// with the swizzle whose span equals the box row (32, 64 or 128 bytes).  Rows past
+// `rows` read as zeros.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int BH, int rows, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int ch = D >= 64 ? 64 : D;
+  const CUtensorMapSwizzle swz = ch * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : ch * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_32B;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint32_t box[3] = {(cuuint32_t)ch, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool supported_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
+bool is16(oattn_dtype t) { return t == OATTN_F16 || t == OATTN_BF16; }
+bool valid_dtype(oattn_dtype t) { return t == OATTN_F16 || t == OATTN_BF16 || t == OATTN_F32; }
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2f = 0.6931471805599453f;
+
+cudaError_t launch_attn(const AttnArgs& a, int block_n, bool bf16, cudaStream_t st) {
+  switch (a.D) {
+    case 16: return launch_attn_d16(a, block_n, bf16, st);
+    case 32: return launch_attn_d32(a, block_n, bf16, st);
+    case 64: return launch_attn_d64(a, block_n, bf16, st);
+    case 128: return launch_attn_d128(a, block_n, bf16, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+oattn_status attn_common_checks(const void* q, const void* k, const void* v, int B, int H, int Nq,
+                                int Nkv, int D, float scale, oattn_dtype dtype) {
+  if (!q || !k || !v) return OATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 0 || Nkv < 0 || D < 1) return OATTN_ERR_INVALID_ARG;
+  if ((long long)B * H > 0x7fffffffLL) return OATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return OATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return OATTN_ERR_INVALID_ARG;
+  if (!is16(dtype)) return OATTN_ERR_UNSUPPORTED;
+  if (!supported_d(D)) return OATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return OATTN_ERR_INVALID_ARG;
+  if (Nq > (1 << 24) || Nkv > (1 << 24)) return OATTN_ERR_UNSUPPORTED;
+  return OATTN_OK;
+}
+
+}  // namespace
+}  // namespace oattn
+
+using namespace oattn;
+
+extern "C" {
+
+int splitk_chunk(int Nkv, int P) {
+  if (Nkv <= 0 || P <= 0) return 0;
+  const long long per = (Nkv + (long long)P - 1) / P;
+  return (int)(((per + 127) / 128) * 128);
+}
+
+const char* oattn_status_string(oattn_status s) {
+  switch (s) {
+    case OATTN_OK: return "ok";
+    case OATTN_ERR_INVALID_ARG: return "invalid argument";
+    case OATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case OATTN_ERR_CUDA: return "CUDA error";
+    case OATTN_ERR_TIMEOUT: return "a bounded device wait gave up";
+    default: return "unknown status";
+  }
+}
+
+oattn_status oattn_device_error(int* code) {
+  if (!code) return OATTN_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* p = status_ptr(&e);
+  if (!p) return OATTN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return OATTN_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return OATTN_ERR_CUDA;
+  *code = (int)v;
+  return v ? OATTN_ERR_TIMEOUT : OATTN_OK;
+}
+
+oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int D, int causal, float scale, oattn_dtype dtype, int block_n,
+                         struct CUstream_st* stream) {
+  oattn_status s = attn_common_checks(q, k, v, B, H, N, N, D, scale, dtype);
+  if (s != OATTN_OK) return s;
+  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4))) return OATTN_ERR_INVALID_ARG;
+  if (block_n == 0) block_n = 128;
+  if (block_n != 32 && block_n != 64 && block_n != 128) return OATTN_ERR_INVALID_ARG;
+  if (N == 0) return OATTN_OK;
+  cudaError_t e;
+  AttnArgs a{};
+  a.status = status_ptr(&e);
+  if (!a.status) return OATTN_ERR_CUDA;
+  const bool bf16 = dtype == OATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, bf16, BH, N, D, 128) || !make_map(&a.tm_k, k, bf16, BH, N, D, block_n) ||
+      !make_map(&a.tm_v, v, bf16, BH, N, D, block_n))
+    return OATTN_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.Nkv = N;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * kLog2e;
+  a.P = 0;
+  a.chunk = 0;
+  a.out_f32 = 0;
+  return launch_attn(a, block_n, bf16, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? OATTN_OK
+             : OATTN_ERR_CUDA;
+}
+
+oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int N, int D, int causal, float scale, oattn_dtype dtype, struct CUstream_st* stream) {
+  return attn_fwd_bn(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, 0, stream);
+}
+
+oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o, float* lse_out,
+                            int P, int rows, int heads, int depth, oattn_dtype in_dtype,
+                            oattn_dtype out_dtype, struct CUstream_st* stream) {
+  if (!o_partial || !lse_partial || !o) return OATTN_ERR_INVALID_ARG;
+  if (P < 1 || P > 256 || rows < 1 || heads < 1 || depth < 1) return OATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return OATTN_ERR_INVALID_ARG;
+  if (!aligned(o_partial, 16) || !aligned(o, 16) || !aligned(lse_partial, 4) ||
+      (lse_out && !aligned(lse_out, 4)))
+    return OATTN_ERR_INVALID_ARG;
+  if (!combine_supported(depth, in_dtype)) return OATTN_ERR_UNSUPPORTED;
+  const long long RH = (long long)rows * heads;
+  return launch_combine(o_partial, lse_partial, o, lse_out, P, RH, depth, in_dtype, out_dtype, 1.0f,
+                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? OATTN_OK
+             : OATTN_ERR_CUDA;
+}
+
+oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                             int H, int Nq, int Nkv, int D, int causal, float scale, oattn_dtype dtype,
+                             int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
+                             struct CUstream_st* stream) {
+  oattn_status s = attn_common_checks(q, k, v, B, H, Nq, Nkv, D, scale, dtype);
+  if (s != OATTN_OK) return s;
+  if (causal && Nq != Nkv) return OATTN_ERR_INVALID_ARG;
+  if (P < 1 || P > 256 || !o_partial || !lse_partial) return OATTN_ERR_INVALID_ARG;
+  if (partial_dtype != OATTN_F32 && partial_dtype != dtype) return OATTN_ERR_INVALID_ARG;
+  if (!aligned(o_partial, 16) || !aligned(lse_partial, 4)) return OATTN_ERR_INVALID_ARG;
+  if (lse && !o) return OATTN_ERR_INVALID_ARG;
+  if (o && (!aligned(o, 16) || (lse && !aligned(lse, 4)))) return OATTN_ERR_INVALID_ARG;
+  if (o && !combine_supported(D, partial_dtype)) return OATTN_ERR_UNSUPPORTED;
+  if (Nq == 0) return OATTN_OK;
+  cudaError_t e;
+  unsigned int* status = status_ptr(&e);
+  if (!status) return OATTN_ERR_CUDA;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const int chunk = splitk_chunk(Nkv, P);
+  const bool bf16 = dtype == OATTN_BF16;
+  cudaError_t le;
+  if (Nq == 1) {
+    // One query row per head: matrix-vector work, streamed on CUDA cores.  (Causal with
+    // Nq == Nkv == 1 sees its single key, the same as non-causal.)
+    DecodeArgs d{};
+    d.q = q; d.k = k; d.v = v;
+    d.o_partial = o_partial;
+    d.lse_partial = lse_partial;
+    d.BH = BH; d.Nkv = Nkv; d.D = D; d.P = P; d.chunk = chunk;
+    d.scale_log2 = scale * kLog2e;
+    d.dtype = dtype;
+    d.partial_dtype = partial_dtype;
+    d.status = status;
+    le = launch_decode(d, st);
+  } else {
+    AttnArgs a{};
+    a.status = status;
+    if (!make_map(&a.tm_q, q, bf16, BH, Nq, D, 128) || !make_map(&a.tm_k, k, bf16, BH, Nkv, D, 128) ||
+        !make_map(&a.tm_v, v, bf16, BH, Nkv, D, 128))
+      return OATTN_ERR_CUDA;
+    a.o = o_partial;
+    a.lse = lse_partial;
+    a.BH = BH; a.N = Nq; a.Nkv = Nkv; a.D = D;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * kLog2e;
+    a.P = P;
+    a.chunk = chunk;
+    a.out_f32 = partial_dtype == OATTN_F32 ? 1 : 0;
+    le = launch_attn(a, 128, bf16, st);
+  }
+  if (le != cudaSuccess) return OATTN_ERR_CUDA;
+  if (o) {
+    le = launch_combine(o_partial, lse_partial, o, lse, P, (long long)BH * Nq, D, partial_dtype, dtype,
+                        kLn2f, st);
+    if (le != cudaSuccess) return OATTN_ERR_CUDA;
+  }
+  return OATTN_OK;
+}
+
+}  // extern "C"

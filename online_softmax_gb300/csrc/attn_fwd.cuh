@@ -1,0 +1,493 @@
+// Tiled attention forward with the online-softmax recurrence on tcgen05 tensor cores.
+//
+// What it computes ("A3. Tiled attention with online normalization", sections "Keep
+// three quantities for each query row" and "Masks that preserve the recurrence";
+// "Streaming attention and online state", section "Online statistics"): for every
+// query row a running maximum m, denominator l and FP32 numerator o are carried over
+// key tiles; each tile gives m' = max(m, rowmax s), alpha = exp(m - m'),
+// p = exp(s - m'), l' = alpha l + rowsum p, o' = alpha o + p V; after the last tile the
+// output is o / l and the row's log-sum-exp is m + log l.  Masked scores (keys past the
+// end, keys after the query when causal, keys outside the split-K partition) are -inf
+// and give p = 0; a row that saw no key ends with l = 0 and stores 0 and -inf.
+//
+// How it maps onto one GB300 SM (one CTA per SM: 193 KB of shared memory and all 512
+// TMEM columns at D = 128):
+//   * A CTA owns two 128-row query tiles of one head (or of one head and split-K
+//     partition).  Warps 0-3 and 4-7 are two softmax warpgroups, one per query tile;
+//     thread r of a warpgroup owns row r, which is TMEM lane r, so row max and row sum
+//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs, warps
+//     10-11 only complete the third warpgroup so that setmaxnreg can move registers
+//     from it to the softmax warpgroups (224 per softmax thread).
+//   * Q tiles are copied once; K and V tiles stream through a ring of shared-memory
+//     slots (K in even, V in odd slots) filled by cp.async.bulk.tensor with the
+//     128/64/32-byte swizzle that matches the tcgen05 shared-memory descriptors.
+//     Keys past the end of the sequence arrive as zeros (out-of-bounds fill).
+//   * S_t = Q_t K^T is a kind::f16 MMA (M=128, N=BN, K=D) into TMEM columns
+//     [t*BN, (t+1)*BN).  The softmax threads read their row (tcgen05.ld), mask with
+//     -inf, take the max, compute p = 2^(s*scale*log2e - m) with one FMA and one
+//     ex2.approx each, sum the FP32 p, round p to the input dtype (cvt.rn, round to
+//     nearest even) and write it back over S (tcgen05.st) as the A operand of
+//     O_t += P V (M=128, N=D, K=BN, A from TMEM, B = V tile read MN-major).
+//   * The issue order S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... lets one
+//     warpgroup's softmax run while the tensor pipe works on the other tile.  A
+//     commit after S_t(j+1) also covers PV_t(j) (commits track every earlier MMA of the
+//     issuing thread), so when the softmax sees S_t(j+1) it may rescale O_t safely.
+//   * The rescale is lazy: a warp keeps its stale maximum until some row's maximum
+//     grows by more than kTau (2^8), so p <= 256, and only then reloads O from TMEM,
+//     multiplies by alpha and stores it back.  Exact arithmetic is unchanged.
+//   * Causal: query tiles are scheduled longest first, wholly-future key tiles are not
+//     visited, and only tiles crossing the diagonal apply the per-element mask.
+//
+// Every wait is bounded (see ptx.cuh); a thread that gives up marks the CTA aborted,
+// everyone leaves its loop, copies and MMAs in flight are drained, TMEM is freed.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace oattn {
+
+constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, p * 2); }
+
+template <int D, int BN>
+struct AttnCfg {
+  static constexpr int D_ = D, BN_ = BN;
+  static constexpr int BM = 128;
+  static constexpr int SW = D * 2 >= 128 ? 128 : D * 2;   // swizzle span = bytes per smem row
+  static constexpr int CH = SW / 2;                        // elements per row chunk (TMA box x)
+  static constexpr int NCH = D / CH;                       // chunks per row
+  static constexpr uint32_t SWZ = SW == 128 ? kSwizzle128B : (SW == 64 ? kSwizzle64B : kSwizzle32B);
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int BUDGET = 200 * 1024;
+  static constexpr int NSLOT_RAW = ((BUDGET - 2 * Q_BYTES) / KV_BYTES) & ~1;
+  static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
+  static constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + NSLOT * KV_BYTES;
+  static constexpr int COL_S0 = 0, COL_S1 = BN, COL_O0 = 2 * BN, COL_O1 = 2 * BN + D;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * BN + 2 * D);
+  static constexpr int THREADS = 384;       // 2 softmax warpgroups + 1 copy/MMA warpgroup
+  static constexpr int REGS_LAUNCH = 168;    // 65536 / 384 rounded down to a multiple of 8
+  static constexpr int REGS_SOFTMAX = 224;   // after setmaxnreg.inc
+  static constexpr int REGS_OTHER = 56;      // after setmaxnreg.dec
+  // Per SM sub-partition: two softmax warps and one other warp share what three warps
+  // had at launch (2*224 + 56 = 3*168).
+  static_assert(2 * REGS_SOFTMAX + REGS_OTHER <= 3 * REGS_LAUNCH, "register split exceeds the launch pool");
+  static_assert(NSLOT >= 4, "need at least two K/V tile pairs in flight");
+  static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+  static_assert(BN % 32 == 0 && D % 16 == 0, "tile shapes");
+};
+
+constexpr float kTauLazy = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Load NC consecutive TMEM columns of this thread's lane as floats (NC % 16 == 0).
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&x)[NC]) {
+  if constexpr (NC % 32 == 0) {
+#pragma unroll
+    for (int c = 0; c < NC / 32; ++c) {
+      uint32_t u[32];
+      tmem_ld_x32(taddr + c * 32, u);
+      tmem_wait_ld_x32(u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[i]);
+    }
+  } else {
+    static_assert(NC == 16, "16 or a multiple of 32 columns");
+    uint32_t u[16];
+    tmem_ld_x16(taddr, u);
+    tmem_wait_ld_x16(u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(u[i]);
+  }
+}
+
+// Multiply NC TMEM columns of this lane by a (read, scale, write back).
+template <int NC>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float a) {
+  constexpr int W = NC % 32 == 0 ? 32 : 16;
+#pragma unroll
+  for (int c = 0; c < NC / W; ++c) {
+    if constexpr (W == 32) {
+      uint32_t u[32];
+      tmem_ld_x32(taddr + c * 32, u);
+      tmem_wait_ld_x32(u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
+      tmem_st_x32(taddr + c * 32, u);
+    } else {
+      uint32_t u[16];
+      tmem_ld_x16(taddr, u);
+      tmem_wait_ld_x16(u);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
+      tmem_st_x16(taddr, u);
+    }
+  }
+}
+
+// Store 16 or 32 output values of a row: 16-bit (rounded to nearest even) or FP32.
+template <int NV, bool BF16>
+__device__ __forceinline__ void store_row_chunk(void* dst, const float (&y)[NV], bool f32) {
+  if (f32) {
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int i = 0; i < NV / 4; ++i) d[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < NV / 8; ++i) {
+      uint4 w;
+      w.x = pack2<BF16>(y[8 * i + 0], y[8 * i + 1]);
+      w.y = pack2<BF16>(y[8 * i + 2], y[8 * i + 3]);
+      w.z = pack2<BF16>(y[8 * i + 4], y[8 * i + 5]);
+      w.w = pack2<BF16>(y[8 * i + 6], y[8 * i + 7]);
+      d[i] = w;
+    }
+  }
+}
+
+// Wait (once) for ring entry n (K_j at n = 2j, V_j at n = 2j+1); `ready` remembers the
+// highest entry already waited for.
+template <int NSLOT>
+__device__ __forceinline__ bool wait_kv(uint64_t* full, int n, int& ready, volatile int* abort,
+                                        unsigned int* status) {
+  if (n <= ready) return true;
+  if (!mbar_wait(&full[n % NSLOT], (uint32_t)(n / NSLOT) & 1u, abort, status, kErrWaitFull)) return false;
+  ready = n;
+  return true;
+}
+
+// S_t = Q_t K_j^T: D/16 MMAs of K = 16 (32 bytes of each operand row), walking the
+// swizzled row chunks.  Descriptors are built per step (no hoisting into registers).
+template <class C, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t q_addr, uint32_t kv_addr, int t, int j,
+                                         uint64_t* bar) {
+  constexpr uint32_t IDESC = idesc_f16(128, C::BN_, BF16, false);
+  constexpr int KPC = C::CH / 16;  // K steps per row chunk
+  const uint32_t k_addr = kv_addr + ((2 * j) % C::NSLOT) * C::KV_BYTES;
+  const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
+  tc_fence_after();
+#pragma unroll 1
+  for (int kk = 0; kk < C::D_ / 16; ++kk) {
+    const uint32_t off = (kk % KPC) * 32;
+    const uint32_t c = kk / KPC;
+    const uint64_t a = smem_desc(q_addr + c * C::BM * C::SW + off, 16, 8 * C::SW, C::SWZ);
+    const uint64_t b = smem_desc(k_addr + c * C::BN_ * C::SW + off, 16, 8 * C::SW, C::SWZ);
+    mma_ss(d, a, b, IDESC, kk > 0 ? 1u : 0u);
+  }
+  tc_commit(bar);
+}
+
+// O_t += P_t V_j: BN/16 MMAs of K = 16 keys, P read from TMEM (8 packed columns per
+// step), V read MN-major (16 key rows per step).
+template <class C, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t kv_addr, int t, int j) {
+  constexpr uint32_t IDESC = idesc_f16(128, C::D_, BF16, true);
+  const uint32_t v_addr = kv_addr + ((2 * j + 1) % C::NSLOT) * C::KV_BYTES;
+  const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
+  const uint32_t p = tmem + (t ? C::COL_S1 : C::COL_S0);
+  tc_fence_after();
+#pragma unroll 1
+  for (int kb = 0; kb < C::BN_ / 16; ++kb) {
+    const uint64_t b = smem_desc(v_addr + kb * 16 * C::SW, C::BN_ * C::SW, 8 * C::SW, C::SWZ);
+    mma_ts(d, p + kb * 8, b, IDESC, (j > 0 || kb > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, int BN, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
+                    float* __restrict__ lse_out, int BH, int N, int Nkv, int causal, float scale_log2,
+                    int P, int chunk, int out_f32, unsigned int* status) {
+  using C = AttnCfg<D, BN>;
+  constexpr int BM = C::BM;
+  constexpr int NSLOT = C::NSLOT;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_full[NSLOT], bar_empty[NSLOT];
+  __shared__ uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2], bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  uint8_t* sQ[2] = {smem, smem + C::Q_BYTES};
+  uint8_t* sKV = smem + 2 * C::Q_BYTES;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- which query tiles, head and key range this CTA owns
+  const bool split = P > 0;
+  const int nparts = split ? P : 1;
+  const int npairs = (N + 2 * BM - 1) / (2 * BM);
+  long long idx = blockIdx.x;
+  const int part = (int)(idx % nparts);
+  idx /= nparts;
+  const int bh = (int)(idx % BH);
+  const int pair_rank = (int)(idx / BH);
+  const int pair = causal ? (npairs - 1 - pair_rank) : pair_rank;
+  const int kv_lo = split ? min(part * chunk, Nkv) : 0;
+  const int kv_hi = split ? min(kv_lo + chunk, Nkv) : Nkv;
+
+  int row0[2], nkv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    row0[t] = pair * 2 * BM + t * BM;
+    nkv[t] = 0;
+    if (row0[t] < N) {
+      const int last_row = min(row0[t] + BM - 1, N - 1);
+      const int key_end = causal ? min(kv_hi, last_row + 1) : kv_hi;
+      nkv[t] = key_end > kv_lo ? (key_end - kv_lo + BN - 1) / BN : 0;
+    }
+  }
+  const int nkv_max = max(nkv[0], nkv[1]);
+
+  // ---- set-up: barriers, TMEM
+  if (warp == 9) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_q, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_o[t], 1);
+    }
+    mbar_init(&bar_done, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort = &s_abort;
+
+  // Registers move from the copy/MMA warpgroup to the softmax warpgroups.  Each
+  // setmaxnreg sits at the top of its role's branch so that the register allocator
+  // sees the new limit for all of that role's code.
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER));
+  if (warp == 8) {
+    // ================================================================ TMA producer
+    if (lane == 0 && nkv_max > 0) {
+      uint32_t qbytes = 0;
+      for (int t = 0; t < 2; ++t) qbytes += nkv[t] > 0 ? C::Q_BYTES : 0;
+      mbar_arrive_expect_tx(&bar_q, qbytes);
+      for (int t = 0; t < 2; ++t)
+        if (nkv[t] > 0)
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sQ[t] + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, row0[t], bh);
+      int issued = 0;
+      for (int n = 0; n < 2 * nkv_max; ++n) {
+        const int slot = n % NSLOT;
+        const uint32_t use = n / NSLOT;
+        if (!mbar_wait(&bar_empty[slot], (use & 1u) ^ 1u, abort, status, kErrWaitLoad)) break;
+        mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
+        const CUtensorMap* map = (n & 1) ? &tm_v : &tm_k;
+        const int key0 = kv_lo + (n >> 1) * BN;
+        uint8_t* dst = sKV + slot * C::KV_BYTES;
+        for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * BN * C::SW, map, &bar_full[slot], c * C::CH, key0, bh);
+        issued = n + 1;
+      }
+      // Drain the copies still in flight before the CTA may exit.
+      mbar_drain(&bar_q, 0, status);
+      for (int n = max(0, issued - NSLOT); n < issued; ++n)
+        mbar_drain(&bar_full[n % NSLOT], (uint32_t)(n / NSLOT) & 1u, status);
+    }
+  } else if (warp == 9) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && nkv_max > 0) {
+      bool ok = mbar_wait(&bar_q, 0, abort, status, kErrWaitFull);
+      int k_ready = -1, v_ready = -1;
+      if (ok) {
+        for (int t = 0; t < 2 && ok; ++t)
+          if (nkv[t] > 0) {
+            ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
+            if (ok) issue_qk<C, BF16>(tmem, smem_u32(sQ[t]), smem_u32(sKV), t, 0, &bar_s[t]);
+          }
+        if (ok) tc_commit(&bar_empty[0]);  // K_0 is free once both S(0) are done
+      }
+      for (int j = 0; ok && j < nkv_max; ++j) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          ok = wait_kv<NSLOT>(bar_full, 2 * j + 1, v_ready, abort, status) &&
+               mbar_wait(&bar_p[t], (uint32_t)j & 1u, abort, status, kErrWaitP);
+          if (!ok) break;
+          issue_pv<C, BF16>(tmem, smem_u32(sKV), t, j);
+          if (j == nkv[t] - 1) tc_commit(&bar_o[t]);
+          if (j + 1 < nkv[t]) {
+            ok = wait_kv<NSLOT>(bar_full, 2 * (j + 1), k_ready, abort, status);
+            if (ok) issue_qk<C, BF16>(tmem, smem_u32(sQ[t]), smem_u32(sKV), t, j + 1, &bar_s[t]);
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bar_empty[(2 * j + 1) % NSLOT]);                      // V_j consumed
+        if (j + 1 < nkv_max) tc_commit(&bar_empty[(2 * j + 2) % NSLOT]);  // K_{j+1} consumed
+      }
+      // Drain every MMA this thread issued before TMEM is released.
+      tc_commit(&bar_done);
+      mbar_drain(&bar_done, 0, status);
+    }
+  }  // warps 10-11: nothing to do
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX));
+    // ================================================================ softmax warpgroups
+    const int t = warp >> 2;   // query tile of this warpgroup
+    const int quad = warp & 3; // TMEM lane quadrant = rows 32*quad .. 32*quad+31
+    const int r = quad * 32 + lane;
+    const int row = row0[t] + r;
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t col_s = t ? C::COL_S1 : C::COL_S0;
+    const uint32_t col_o = t ? C::COL_O1 : C::COL_O0;
+    float m = -INFINITY;  // running max in use, log2 units of scale*s
+    float l = 0.f;
+    bool ok = true;
+
+    if (row0[t] < N) {
+      for (int j = 0; j < nkv[t]; ++j) {
+        ok = mbar_wait(&bar_s[t], (uint32_t)j & 1u, abort, status, kErrWaitS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float s[BN];
+        tmem_load_cols<BN>(trow + col_s, s);
+
+        const int key0 = kv_lo + j * BN;
+        const bool need_mask = (key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0[t]);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const int key = key0 + c;
+            const bool vis = key < kv_hi && (!causal || key <= row);
+            s[c] = vis ? s[c] : -INFINITY;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        const float mnew = fmaxf(m, mx * scale_log2);
+        const bool grow = (mnew - m) > kTauLazy;  // false for -inf - -inf (NaN)
+        const bool rescale = __any_sync(0xffffffffu, grow);
+        const float m_use = rescale ? mnew : m;
+        const float alpha = (m_use == m) ? 1.f : ex2(m - m_use);  // ex2(-inf) = 0
+        if (rescale && j > 0) {
+          tmem_scale_cols<D>(trow + col_o, alpha);
+          tmem_wait_st();
+        }
+        const float base = (m_use == -INFINITY) ? 0.f : m_use;
+        float rowsum = 0.f;
+#pragma unroll
+        for (int c2 = 0; c2 < BN / 32; ++c2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(s[c2 * 32 + 2 * i], scale_log2, -base));
+            const float p1 = ex2(fmaf(s[c2 * 32 + 2 * i + 1], scale_log2, -base));
+            rowsum += p0 + p1;
+            pk[i] = pack2<BF16>(p0, p1);
+          }
+          tmem_st_x16(trow + col_s + c2 * 16, pk);
+        }
+        tmem_wait_st();
+        l = fmaf(alpha, l, rowsum);
+        m = m_use;
+        tc_fence_before();
+        mbar_arrive(&bar_p[t]);
+      }
+
+      // ---- epilogue: o / l and the log-sum-exp of the row
+      if (ok && nkv[t] > 0) {
+        ok = mbar_wait(&bar_o[t], 0, abort, status, kErrWaitO);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const bool f32 = split && out_f32;
+        const size_t plane = split ? (size_t)part * BH * N : 0;
+        const size_t grow_idx = plane + (size_t)bh * N + row;
+        const size_t esz = f32 ? 4 : 2;
+        uint8_t* dst = static_cast<uint8_t*>(out) + grow_idx * D * esz;
+        constexpr int W = D % 32 == 0 ? 32 : 16;
+        if (nkv[t] > 0) tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / W; ++c) {
+          float y[W];
+          if (nkv[t] > 0) {
+            tmem_load_cols<W>(trow + col_o + c * W, y);
+#pragma unroll
+            for (int i = 0; i < W; ++i) y[i] = y[i] * inv + 0.f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) y[i] = 0.f;
+          }
+          if (row < N) store_row_chunk<W, BF16>(dst + (size_t)c * W * esz, y, f32);
+        }
+        if (row < N && lse_out != nullptr) {
+          const float lse2 = (l > 0.f) ? m + lg2(l) : -INFINITY;
+          lse_out[grow_idx] = split ? lse2 : lse2 * kLn2;
+        }
+      }
+    }
+  }
+
+  // ---- tear-down: everyone is done with TMEM before it is released
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, int BN, bool BF16>
+cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
+  using C = AttnCfg<D, BN>;
+  auto kern = attn_fwd_kernel<D, BN, BF16>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    // The setmaxnreg split draws on the registers the CTA was launched with: refuse to
+    // launch a build whose register count would make setmaxnreg.inc wait forever.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < C::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long npairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  const long long blocks = npairs * a.BH * (a.P > 0 ? a.P : 1);
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.BH, a.N,
+                                                           a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
+                                                           a.out_f32, a.status);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t st) {
+  switch (block_n) {
+    case 32: return bf16 ? launch_attn_inst<D, 32, true>(a, st) : launch_attn_inst<D, 32, false>(a, st);
+    case 64: return bf16 ? launch_attn_inst<D, 64, true>(a, st) : launch_attn_inst<D, 64, false>(a, st);
+    case 128: return bf16 ? launch_attn_inst<D, 128, true>(a, st) : launch_attn_inst<D, 128, false>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace oattn

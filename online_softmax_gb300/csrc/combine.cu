@@ -1,0 +1,270 @@
+// Split-K LSE-weighted combine ("fa4_splitk_combine", the Mojo module doc for the SM100
+// workspace combine): one warp per output row-head rh, reducing over P partitions
+//   m* = max_p lse_p,  G = log2(sum_p 2^(lse_p - m*)) + m*,
+//   scale_p = 2^(lse_p - G),  O[d] = sum_p scale_p * o_partial[p, rh, d].
+//
+// Structure on GB300: the LSE reduction is done once per warp into per-lane
+// registers (lane l keeps partitions l, l+32, ...; five xor shuffles for the max and
+// five for the sum); each partition's scale is then broadcast from its owning lane
+// with one indexed shuffle, and the depth vector of the next partition step is loaded
+// (128-bit loads) before the current one is folded in.  When a partition row is
+// shorter than a warp of 128-bit vectors (16-bit data, depth 128), the warp splits into
+// 32/LPP groups that take consecutive partitions and are summed at the end.  Ladder
+// sizes P in {2, 4, 8, 16, 32} get fully unrolled instances; any other P runs the
+// runtime-bound loop.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace oattn {
+namespace {
+
+constexpr int kCombineWarps = 8;  // row-heads per 256-thread block
+constexpr int kMaxP = 256;
+constexpr int kLseSlots = kMaxP / 32;
+
+template <typename T> struct Vec;  // one 16-byte vector of T
+template <> struct Vec<float> { static constexpr int E = 4; };
+template <> struct Vec<__nv_bfloat16> { static constexpr int E = 8; };
+template <> struct Vec<__half> { static constexpr int E = 8; };
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float (&x)[Vec<T>::E]) {
+  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+  if constexpr (Vec<T>::E == 4) {
+    x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+  } else {
+    constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = unpack_lo<BF>(w[i]);
+      x[2 * i + 1] = unpack_hi<BF>(w[i]);
+    }
+  }
+}
+
+template <typename T, int E>
+__device__ __forceinline__ void store_vec(T* p, const float (&x)[E]) {
+  if constexpr (std::is_same<T, float>::value) {
+#pragma unroll
+    for (int i = 0; i < E; i += 4)
+      *reinterpret_cast<float4*>(p + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+  } else {
+    constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+    if constexpr (E == 8) {
+      uint4 u;
+      u.x = pack2<BF>(x[0], x[1]); u.y = pack2<BF>(x[2], x[3]);
+      u.z = pack2<BF>(x[4], x[5]); u.w = pack2<BF>(x[6], x[7]);
+      *reinterpret_cast<uint4*>(p) = u;
+    } else {
+      uint2 u;
+      u.x = pack2<BF>(x[0], x[1]); u.y = pack2<BF>(x[2], x[3]);
+      *reinterpret_cast<uint2*>(p) = u;
+    }
+  }
+}
+
+// TIn/TOut element types; LPP lanes per partition row; VPL 16-byte vectors per lane;
+// P_STATIC > 0: exact partition count, fully unrolled; 0: runtime P (<= kMaxP).
+template <typename TIn, typename TOut, int LPP, int VPL, int P_STATIC>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    splitk_combine_kernel(const TIn* __restrict__ o_partial, const float* __restrict__ lse_partial,
+                          TOut* __restrict__ out, float* __restrict__ lse_out, int P_rt,
+                          long long RH, float lse_scale) {
+  constexpr int E = Vec<TIn>::E;
+  constexpr int PPS = 32 / LPP;               // partitions folded per step
+  constexpr int DEPTH = LPP * VPL * E;
+  constexpr int SLOTS = P_STATIC > 0 ? (P_STATIC + 31) / 32 : kLseSlots;
+  const int P = P_STATIC > 0 ? P_STATIC : P_rt;
+
+  const int lane = threadIdx.x & 31;
+  const long long rh = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (rh >= RH) return;  // whole warp leaves together
+
+  // ---- LSE reduction, once, into per-lane registers
+  float lse[SLOTS];
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int p = s * 32 + lane;
+    lse[s] = (p < P) ? __ldg(lse_partial + (long long)p * RH + rh) : -INFINITY;
+    m = fmaxf(m, lse[s]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const bool dead = (m == -INFINITY);
+  const float msafe = dead ? 0.f : m;
+  float sum = 0.f;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) sum += ex2(lse[s] - msafe);  // ex2(-inf) = +0
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float G = dead ? -INFINITY : lg2(sum) + msafe;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) lse[s] = dead ? 0.f : ex2(lse[s] - G);  // now scale_p
+
+  // ---- weighted accumulation with the next step's vectors prefetched
+  const int sub = lane / LPP;  // which partition of the step this lane folds
+  const int li = lane % LPP;
+  float acc[VPL][E];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
+
+  const TIn* base = o_partial + rh * DEPTH + li * E;
+  const long long pstride = RH * (long long)DEPTH;
+  const int steps = (P + PPS - 1) / PPS;
+
+  float cur[VPL][E], nxt[VPL][E];
+  auto fetch = [&](int step, float (&x)[VPL][E]) {
+    const int p = step * PPS + sub;
+    if (p < P) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) load_vec<TIn>(base + p * pstride + v * LPP * E, x[v]);
+    } else {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[v][e] = 0.f;
+    }
+  };
+  auto fold = [&](float sc, float (&x)[VPL][E]) {
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[v][e] = fmaf(sc, (sc != 0.f) ? x[v][e] : 0.f, acc[v][e]);
+  };
+
+  fetch(0, cur);
+  if constexpr (P_STATIC > 0) {
+#pragma unroll
+    for (int step = 0; step < (P_STATIC + PPS - 1) / PPS; ++step) {
+      const int p = step * PPS + sub;
+      const float sc = __shfl_sync(0xffffffffu, lse[(step * PPS) / 32], p & 31);
+      if (step + 1 < steps) fetch(step + 1, nxt);
+      fold(p < P ? sc : 0.f, cur);
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+#pragma unroll
+        for (int e = 0; e < E; ++e) cur[v][e] = nxt[v][e];
+    }
+  } else {
+    // Runtime P: a partition's scale would need a run-time register index, so the
+    // warp parks its per-lane scales in its own shared-memory row instead and every
+    // lane reads the one it needs (a broadcast read).
+    __shared__ float s_scale[kCombineWarps][kMaxP];
+    float* my = s_scale[threadIdx.x >> 5];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s)
+      if (s * 32 + lane < P) my[s * 32 + lane] = lse[s];
+    __syncwarp();
+#pragma unroll 1
+    for (int step = 0; step < steps; ++step) {
+      const int p = step * PPS + sub;
+      const float sc = p < P ? my[p] : 0.f;
+      if (step + 1 < steps) fetch(step + 1, nxt);
+      fold(sc, cur);
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+#pragma unroll
+        for (int e = 0; e < E; ++e) cur[v][e] = nxt[v][e];
+    }
+  }
+
+  // ---- fold the PPS partition groups of the warp together and store
+#pragma unroll
+  for (int o = LPP; o < 32; o <<= 1)
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[v][e] += __shfl_xor_sync(0xffffffffu, acc[v][e], o);
+
+  if (sub == 0) {
+    TOut* dst = out + rh * DEPTH + li * E;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      float y[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) y[e] = dead ? 0.f : acc[v][e] + 0.f;
+      store_vec<TOut, E>(dst + v * LPP * E, y);
+    }
+  }
+  if (lse_out != nullptr && lane == 0) lse_out[rh] = dead ? -INFINITY : G * lse_scale;
+}
+
+template <typename TIn, typename TOut, int LPP, int VPL>
+cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
+                     float lse_scale, cudaStream_t st) {
+  const dim3 grid((unsigned)((RH + kCombineWarps - 1) / kCombineWarps));
+  const dim3 block(kCombineWarps * 32);
+  auto* a = static_cast<const TIn*>(op);
+  auto* c = static_cast<TOut*>(o);
+  switch (P) {
+    case 2: splitk_combine_kernel<TIn, TOut, LPP, VPL, 2><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    case 4: splitk_combine_kernel<TIn, TOut, LPP, VPL, 4><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    case 8: splitk_combine_kernel<TIn, TOut, LPP, VPL, 8><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    case 16: splitk_combine_kernel<TIn, TOut, LPP, VPL, 16><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    case 32: splitk_combine_kernel<TIn, TOut, LPP, VPL, 32><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    default: splitk_combine_kernel<TIn, TOut, LPP, VPL, 0><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+  }
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_depth(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
+                         int depth, float lse_scale, cudaStream_t st) {
+  constexpr int E = Vec<TIn>::E;
+  const int nvec = depth / E;  // 16-byte vectors per partition row
+  switch (nvec) {
+    case 2: return launch_p<TIn, TOut, 2, 1>(op, lp, o, lo, P, RH, lse_scale, st);
+    case 4: return launch_p<TIn, TOut, 4, 1>(op, lp, o, lo, P, RH, lse_scale, st);
+    case 8: return launch_p<TIn, TOut, 8, 1>(op, lp, o, lo, P, RH, lse_scale, st);
+    case 16: return launch_p<TIn, TOut, 16, 1>(op, lp, o, lo, P, RH, lse_scale, st);
+    case 32: return launch_p<TIn, TOut, 32, 1>(op, lp, o, lo, P, RH, lse_scale, st);
+    case 64: return launch_p<TIn, TOut, 32, 2>(op, lp, o, lo, P, RH, lse_scale, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename TIn>
+cudaError_t launch_out(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
+                       int depth, int out_dt, float lse_scale, cudaStream_t st) {
+  switch (out_dt) {
+    case kF32: return launch_depth<TIn, float>(op, lp, o, lo, P, RH, depth, lse_scale, st);
+    case kBF16: return launch_depth<TIn, __nv_bfloat16>(op, lp, o, lo, P, RH, depth, lse_scale, st);
+    case kF16: return launch_depth<TIn, __half>(op, lp, o, lo, P, RH, depth, lse_scale, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool combine_supported(int depth, int in_dt) {
+  const int E = (in_dt == kF32) ? 4 : 8;
+  if (depth % E) return false;
+  const int nvec = depth / E;
+  return nvec == 2 || nvec == 4 || nvec == 8 || nvec == 16 || nvec == 32 || nvec == 64;
+}
+
+cudaError_t launch_combine(const void* o_partial, const float* lse_partial, void* o, float* lse_out,
+                           int P, long long RH, int depth, int in_dt, int out_dt, float lse_scale,
+                           cudaStream_t st) {
+  if (RH <= 0) return cudaSuccess;
+  switch (in_dt) {
+    case kF32: return launch_out<float>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, st);
+    case kBF16: return launch_out<__nv_bfloat16>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, st);
+    case kF16: return launch_out<__half>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace oattn

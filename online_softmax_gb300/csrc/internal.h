@@ -1,0 +1,50 @@
+// Launchers shared between the translation units of the library (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace oattn {
+
+enum DType : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
+
+// ---- splitk_combine (combine.cu)
+bool combine_supported(int depth, int in_dt);
+cudaError_t launch_combine(const void* o_partial, const float* lse_partial, void* o,
+                           float* lse_out, int P, long long RH, int depth, int in_dt, int out_dt,
+                           float lse_scale, cudaStream_t st);
+
+// ---- one-query split-K decode on CUDA cores (decode.cu)
+struct DecodeArgs {
+  const void* q;       // [BH, D]
+  const void* k;       // [BH, Nkv, D]
+  const void* v;       // [BH, Nkv, D]
+  void* o_partial;     // [P, BH, D] f32 or input dtype
+  float* lse_partial;  // [P, BH] base 2
+  long long BH;
+  int Nkv, D, P, chunk;
+  float scale_log2;    // scale * log2(e)
+  int dtype;           // kF16 / kBF16
+  int partial_dtype;   // kF32 / input dtype
+  unsigned int* status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+
+// ---- tcgen05 attention forward / split-K partitions (attn_fwd_d*.cu)
+struct AttnArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [BH, N, D], boxes of 128 or BN rows
+  void* o;            // plain: [BH, N, D] dtype;  split: [P, BH*N, D] partial dtype
+  float* lse;         // plain: [BH, N] natural log (nullable);  split: [P, BH*N] base 2
+  int BH, N, Nkv, D;
+  int causal;
+  float scale_log2;
+  int P, chunk;       // split mode when P > 0
+  int out_f32;        // split mode: o_partial is float32
+  unsigned int* status;
+};
+// Instantiated per head dimension in attn_fwd_d{16,32,64,128}.cu.
+cudaError_t launch_attn_d16(const AttnArgs& a, int block_n, int bf16, cudaStream_t st);
+cudaError_t launch_attn_d32(const AttnArgs& a, int block_n, int bf16, cudaStream_t st);
+cudaError_t launch_attn_d64(const AttnArgs& a, int block_n, int bf16, cudaStream_t st);
+cudaError_t launch_attn_d128(const AttnArgs& a, int block_n, int bf16, cudaStream_t st);
+
+}  // namespace oattn

@@ -51,23 +51,36 @@ def mix64(z: np.ndarray) -> np.ndarray:
     return z ^ (z >> np.uint64(31))
 
 
-def words(seed: int, stream: int, start: int, count: int) -> np.ndarray:
-    """Raw 64-bit words for elements [start, start+count) of (seed, stream)."""
+def words_at(seed: int, stream: int, idx) -> np.ndarray:
+    """Raw 64-bit words for arbitrary element indices of (seed, stream)."""
     if not (0 <= stream < 256 and 0 <= seed < 2**16):
         raise ValueError("stream must be < 256 and seed < 2**16")
-    if start < 0 or start + count > 2**40:
+    idx = np.asarray(idx, dtype=np.int64)
+    if idx.size and (idx.min() < 0 or idx.max() >= 2**40):
         raise ValueError("element index out of the stream's 2**40 block")
     base = np.uint64((1 + stream * 2**40 + seed * 2**48) % 2**64)
-    idx = np.arange(start, start + count, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        ctr = (idx + base) * GAMMA
+        ctr = (idx.astype(np.uint64) + base) * GAMMA
     return mix64(ctr)
+
+
+def words(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Raw 64-bit words for elements [start, start+count) of (seed, stream)."""
+    return words_at(seed, stream, np.arange(start, start + count, dtype=np.int64))
+
+
+def normal_at(seed: int, stream: int, idx, mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
+    """float32 approximately-normal values at arbitrary element indices."""
+    return _irwin_hall(words_at(seed, stream, idx), mu, sigma)
 
 
 def normal(seed: int, stream: int, start: int, count: int,
            mu: float = 0.0, sigma: float = 1.0) -> np.ndarray:
     """float32 approximately-normal values (Irwin-Hall of four 16-bit fields)."""
-    w = words(seed, stream, start, count)
+    return _irwin_hall(words(seed, stream, start, count), mu, sigma)
+
+
+def _irwin_hall(w: np.ndarray, mu: float, sigma: float) -> np.ndarray:
     m16 = np.uint64(0xFFFF)
     s = ((w & m16) + ((w >> np.uint64(16)) & m16)
          + ((w >> np.uint64(32)) & m16) + (w >> np.uint64(48)))
@@ -141,5 +154,24 @@ def lse_partials(seed: int, P: int, RH: int, start_rh: int = 0, count_rh: int | 
         v = normal(seed, STREAM_LSE, s, count_rh, mu, sigma)
         d = bernoulli(seed, STREAM_LSE_DROP, s, count_rh, drop)
         v[d | dead] = -np.inf
+        out[p] = v
+    return out
+
+
+def bernoulli_at(seed: int, stream: int, idx, prob: float) -> np.ndarray:
+    thresh = np.uint64(int(np.floor(prob * 2**32)))
+    return (words_at(seed, stream, idx) >> np.uint64(32)) < thresh
+
+
+def lse_partials_at(seed: int, P: int, RH: int, rh_idx, mu: float = 10.0, sigma: float = 2.0,
+                    drop: float = 0.05, row_drop: float = 0.001) -> np.ndarray:
+    """lse_partials restricted to the row-heads `rh_idx`: float32 [P, len(rh_idx)]."""
+    rh_idx = np.asarray(rh_idx, dtype=np.int64)
+    dead = bernoulli_at(seed, STREAM_ROW_DROP, rh_idx, row_drop)
+    out = np.empty((P, len(rh_idx)), dtype=np.float32)
+    for p in range(P):
+        j = p * RH + rh_idx
+        v = normal_at(seed, STREAM_LSE, j, mu, sigma)
+        v[bernoulli_at(seed, STREAM_LSE_DROP, j, drop) | dead] = -np.inf
         out[p] = v
     return out

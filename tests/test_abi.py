@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and exports every
+function the header declares, the split-K chunk rule matches the oracle's reading, and
+invalid arguments are refused before anything touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "oattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import online_softmax_gb300 as ops
+    from online_softmax_gb300 import build as b
+    if not os.path.exists(ops.library_path):
+        b.build()
+    return ops.lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:oattn_status|int|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "splitk_combine", "splitk_chunk",
+              "oattn_status_string", "oattn_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(__import__("online_softmax_gb300").library_path)
+    for n in declared_functions():
+        assert hasattr(raw, n), f"{n} declared in oattn.h but not exported"
+
+
+@pytest.mark.parametrize("nkv", [0, 1, 127, 128, 1000, 4096, 32768, 100000])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16, 37, 256])
+def test_chunk_matches_oracle_reading(lib, nkv, P):
+    c = lib.splitk_chunk(nkv, P)
+    if nkv == 0:
+        assert c == 0
+        return
+    b = oracle.splitk_bounds(nkv, P, 128)
+    assert b[0] == (0, min(c, nkv))
+    assert all(hi - lo == c for lo, hi in b if hi < nkv)
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.oattn_status_string(s)
+
+
+# Non-null stand-in addresses, 16-byte aligned or not; never dereferenced because every
+# call below fails argument validation first.
+A = ctypes.c_void_p(0x1000)
+A2 = ctypes.c_void_p(0x2000)
+MIS = ctypes.c_void_p(0x1002)
+
+
+def attn(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A2, lse=None, B=1, H=1, N=16, D=64, causal=0, scale=0.125, dt=1, bn=0)
+    a.update(kw)
+    return lib.attn_fwd_bn(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                           a["causal"], a["scale"], a["dt"], a["bn"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(B=0), 1), (dict(N=-1), 1), (dict(scale=0.0), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1), (dict(dt=7), 1), (dict(dt=2), 2),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(q=MIS), 1), (dict(o=MIS), 1), (dict(bn=48), 1),
+    (dict(lse=ctypes.c_void_p(0x1001)), 1),
+])
+def test_attn_fwd_rejects(lib, kw, expect):
+    assert attn(lib, **kw) == expect
+
+
+def splitk(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=None, lse=None, B=1, H=1, Nq=1, Nkv=64, D=128, causal=0, scale=0.1, dt=1,
+             P=4, op=A2, lp=A2, pdt=2)
+    a.update(kw)
+    return lib.attn_fwd_splitk(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nkv"],
+                               a["D"], a["causal"], a["scale"], a["dt"], a["P"], a["op"], a["lp"], a["pdt"],
+                               None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(P=0), 1), (dict(P=257), 1), (dict(op=None), 1), (dict(lp=None), 1),
+    (dict(causal=1, Nq=2, Nkv=3), 1), (dict(pdt=0), 1), (dict(lse=A), 1), (dict(D=48), 2),
+    (dict(op=MIS), 1), (dict(k=None), 1),
+])
+def test_splitk_rejects(lib, kw, expect):
+    assert splitk(lib, **kw) == expect
+
+
+def combine(lib, **kw):
+    a = dict(op=A, lp=A, o=A2, lo=None, P=4, rows=8, heads=2, depth=128, idt=2, odt=2)
+    a.update(kw)
+    return lib.splitk_combine(a["op"], a["lp"], a["o"], a["lo"], a["P"], a["rows"], a["heads"], a["depth"],
+                              a["idt"], a["odt"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(op=None), 1), (dict(o=None), 1), (dict(P=0), 1), (dict(P=300), 1), (dict(rows=0), 1),
+    (dict(depth=100), 2), (dict(depth=8, idt=1), 2), (dict(depth=2048), 2), (dict(idt=5), 1), (dict(op=MIS), 1),
+])
+def test_combine_rejects(lib, kw, expect):
+    assert combine(lib, **kw) == expect
+
+
+def test_device_error_needs_pointer(lib):
+    assert lib.oattn_device_error(None) == 1

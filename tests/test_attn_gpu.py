@@ -1,0 +1,140 @@
+"""Parity of attn_fwd (tcgen05/TMA kernel, through the C ABI) against the FP64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+ops = pytest.importorskip("online_softmax_gb300")
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    assert ops.device_error() == 0, "a bounded device wait gave up"
+
+
+def run_attn(q, k, v, causal, block_n=0, scale=None, with_lse=True):
+    B, Hh, N, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hh, N), dtype=torch.float32, device=q.device) if with_lse else None
+    ops.attn_fwd_bn(q, k, v, o, lse, causal=causal, scale=scale, block_n=block_n)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def check_full(qb, kb, vb, dtype, causal, block_n=0, scale=None, what=""):
+    D = qb.shape[-1]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    q, k, v = (H.to_device(x, dtype) for x in (qb, kb, vb))
+    o, lse = run_attn(q, k, v, causal, block_n, scale)
+    O_ref, L_ref = oracle.attention(synth.to_f64(qb, dtype), synth.to_f64(kb, dtype),
+                                    synth.to_f64(vb, dtype), scale, causal)
+    H.check16(H.to_f64(o), O_ref, what + " O")
+    H.check32(H.to_f64(lse), L_ref, what + " LSE")
+
+
+def test_single_head_n128_d64():
+    """B=1, H=1, N=128, D=64, bf16, non-causal, scale 1/sqrt(D)."""
+    qb, kb, vb = H.qkv_host(1, 1, 1, 128, 64, "bf16")
+    check_full(qb, kb, vb, "bf16", False, what="n128")
+
+
+# Workshop checker matrix: D x N x dtype x causal x BN, three value regimes.
+@pytest.mark.parametrize("regime", ["normal", "uniform", "large"])
+@pytest.mark.parametrize("block_n", [32, 64])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 1000, 2048])
+@pytest.mark.parametrize("D", [16, 32, 64])
+def test_workshop_sweep(D, N, dtype, causal, block_n, regime):
+    seed = 100 + D + N % 7
+    qb, kb, vb = H.qkv_host(seed, 1, 1, N, D, dtype)
+    if regime == "uniform":
+        qb = synth.round_to(np.zeros(qb.shape, np.float32), dtype)
+    elif regime == "large":  # Q scaled by 8 (a power of two: exact in both dtypes)
+        qb = synth.round_to((synth.to_f64(qb, dtype) * 8.0).astype(np.float32), dtype)
+    check_full(qb, kb, vb, dtype, causal, block_n, what=f"D{D} N{N} {dtype} c{causal} bn{block_n} {regime}")
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_default_tile_multihead_ragged(D, causal):
+    qb, kb, vb = H.qkv_host(7, 2, 3, 333, D, "bf16")
+    check_full(qb, kb, vb, "bf16", causal, what=f"D{D} multihead")
+
+
+@pytest.mark.parametrize("block_n", [32, 64, 128])
+def test_d128_tiles_and_scale(block_n):
+    qb, kb, vb = H.qkv_host(8, 1, 2, 700, 128, "f16")
+    check_full(qb, kb, vb, "f16", True, block_n, scale=0.3, what=f"d128 bn{block_n}")
+
+
+def test_lse_optional_and_n_zero():
+    qb, kb, vb = H.qkv_host(9, 1, 1, 200, 64, "bf16")
+    q, k, v = (H.to_device(x, "bf16") for x in (qb, kb, vb))
+    o1, l1 = run_attn(q, k, v, True)
+    o2, _ = run_attn(q, k, v, True, with_lse=False)
+    assert torch.equal(o1, o2)
+    z = torch.empty((1, 1, 0, 64), dtype=torch.bfloat16, device="cuda")
+    ops.attn_fwd(z, z, z, torch.empty_like(z), None)
+
+
+def test_causal_future_perturbation_bitwise():
+    """Changing K and V rows at and after j leaves every earlier causal row bit-identical."""
+    N, D = 1000, 64
+    qb, kb, vb = H.qkv_host(11, 1, 2, N, D, "bf16")
+    q, k, v = (H.to_device(x, "bf16") for x in (qb, kb, vb))
+    o, lse = run_attn(q, k, v, True)
+    for j in (1, 300, 512, 999):
+        k2, v2 = k.clone(), v.clone()
+        k2[:, :, j:] = torch.randn_like(k2[:, :, j:])
+        v2[:, :, j:] = torch.randn_like(v2[:, :, j:])
+        o2, lse2 = run_attn(q, k2, v2, True)
+        assert torch.equal(o2[:, :, :j], o[:, :, :j]), f"row < {j} changed"
+        assert torch.equal(lse2[:, :, :j], lse[:, :, :j])
+        assert not torch.equal(o2[:, :, j:], o[:, :, j:])
+
+
+# ---- full prefill size: B=4, H=32, N=4096, D=128, bf16 (inputs drawn on the device)
+PREFILL = dict(B=4, H=32, N=4096, D=128, seed=3)
+
+
+def prefill_inputs(dtype="bf16"):
+    import synth.cuda as sc
+    B, Hh, N, D, seed = (PREFILL[x] for x in ("B", "H", "N", "D", "seed"))
+    t = lambda: torch.empty((B, Hh, N, D), dtype=H.torch_dtype(dtype), device="cuda")
+    q = sc.fill_normal(t(), seed, synth.STREAM_Q, dtype)
+    k = sc.fill_normal(t(), seed, synth.STREAM_K, dtype)
+    v = sc.fill_normal(t(), seed, synth.STREAM_V, dtype)
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_full_size_sampled(causal):
+    B, Hh, N, D, seed = (PREFILL[x] for x in ("B", "H", "N", "D", "seed"))
+    q, k, v = prefill_inputs()
+    o, lse = run_attn(q, k, v, causal)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.r_[0, 1, 127, 128, 255, 256, 2047, 4095, rng.integers(0, N, 56)])
+    for bh in (0, 37, B * Hh - 1):
+        qr = H.head_slice(seed, synth.STREAM_Q, bh, N, D, "bf16", rows)
+        kh = H.head_slice(seed, synth.STREAM_K, bh, N, D, "bf16")
+        vh = H.head_slice(seed, synth.STREAM_V, bh, N, D, "bf16")
+        O_ref, L_ref = oracle.attention_rows(qr, rows, kh, vh, 1.0 / math.sqrt(D), causal)
+        b, h = divmod(bh, Hh)
+        H.check16(H.to_f64(o[b, h, rows]), O_ref, f"prefill bh{bh} O")
+        H.check32(H.to_f64(lse[b, h, rows]), L_ref, f"prefill bh{bh} LSE")
+
+
+def test_prefill_deterministic():
+    q, k, v = prefill_inputs()
+    o1, l1 = run_attn(q, k, v, True)
+    o2, l2 = run_attn(q, k, v, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
