@@ -158,7 +158,6 @@ class ClockSampler:
 def oracle_sample(budget_s: float, max_heads: int = B * H):
     """Time the FP64 oracle on whole heads of the prefill workload until `budget_s` of
     CPU work has run.  Returns (TFLOP/s, seconds, heads)."""
-    import numpy as np
     import oracle
     import synth
     from tests import helpers as Hl
@@ -173,34 +172,49 @@ def oracle_sample(budget_s: float, max_heads: int = B * H):
         t_total += time.perf_counter() - t0
         done += 1
         del qh, kh, vh
-        np.empty(0)
     flops = 4.0 * D * N * (N + 1) / 2 * done
     return flops / t_total / 1e12, t_total, done
 
 
 def run_reference(args):
+    """The reference arm: the FP64 oracle on the host cores.  One step = the oracle on
+    R query rows (the last R of one head, so each row sees ~N keys) with R chosen so the
+    whole --warmup + --steps run stays near 90 s of CPU time."""
+    import numpy as np
+    import oracle
+    import synth
+    from tests import helpers as Hl
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    # one step = the oracle on one whole head of the workload (bounded CPU work)
+    kh = Hl.head_slice(SEED, synth.STREAM_K, 0, N, D, "bf16")
+    vh = Hl.head_slice(SEED, synth.STREAM_V, 0, N, D, "bf16")
+
+    def run(rows):
+        qr = Hl.head_slice(SEED, synth.STREAM_Q, 0, N, D, "bf16", rows)
+        t0 = time.perf_counter()
+        oracle.attention_rows(qr, rows, kh, vh, 1.0 / math.sqrt(D), CAUSAL)
+        return time.perf_counter() - t0
+
+    cal = np.arange(N - 256, N)
+    t_row = min(run(cal) for _ in range(2)) / len(cal)
+    R = int(min(N, max(16, 90.0 / (args.steps + args.warmup) / t_row)))
+    rows = np.arange(N - R, N)
+    flops_step = 4.0 * D * float(np.sum(rows + 1))  # causal: row i sees i+1 keys
     for _ in range(args.warmup):
-        oracle_sample(0.0, max_heads=1)
-    times = []
-    for _ in range(args.steps):
-        _, t, _ = oracle_sample(0.0, max_heads=1)
-        times.append(t)
+        run(rows)
+    times = [run(rows) for _ in range(args.steps)]
     per_step = sum(times) / len(times)
-    flops_step = 4.0 * D * N * (N + 1) / 2
     value = flops_step / per_step / 1e12
     cores = os.cpu_count()
+    sample = (f"last {R} query rows of one head of the workload per step (4096 keys, causal, D=128), "
+              "FP64 numpy oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
-                   "sample": "one head (4096 queries x 4096 keys) per step"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "one whole head of the workload per step, FP64 numpy oracle"},
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -214,7 +228,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="headline only (no combine/decode/e2e)")
+    ap.add_argument("--part", default="all", choices=["all", "attn", "combine", "decode"],
+                    help="all (default) or one measurement alone, e.g. for a profiler run")
+    ap.add_argument("--combine-P", default="2,8,16,32,37")
+    ap.add_argument("--combine-dtype", default="f32,bf16")
+    ap.add_argument("--decode-batch", type=int, default=64)
+    ap.add_argument("--decode-P", default="4,8,16,37")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.impl == "reference":
@@ -236,6 +255,34 @@ def main():
 
     stream = torch.cuda.current_stream()
     pk, pk_kind = peaks()
+
+    line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": world, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+    if args.part in ("all", "attn"):
+        line.update(measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank))
+    if args.part in ("all", "combine"):
+        line["combine"] = measure_combine(torch, ops, sc, synth, pk, dev,
+                                          [int(x) for x in args.combine_P.split(",")],
+                                          args.combine_dtype.split(","))
+    if args.part in ("all", "decode"):
+        line["decode_splitk"] = measure_decode(torch, ops, sc, synth, pk, dev, args.decode_batch,
+                                               [int(x) for x in args.decode_P.split(",")])
+    torch.cuda.empty_cache()
+    if rank == 0 and args.part == "all" and not args.no_cpu_baseline:
+        tf, secs, heads = oracle_sample(12.0)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{heads} whole heads (4096x4096 causal, D=128) of the workload, "
+                                          f"FP64 numpy oracle, {secs:.1f} s"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
+    """Headline: K timed attention steps on resident inputs, then the end-to-end variant."""
+    stream = torch.cuda.current_stream()
 
     # ---- inputs of the prefill workload, resident in HBM
     def rand(stream_id):
@@ -270,9 +317,7 @@ def main():
     achieved = FLOPS / per_launch_s / 1e12
     traffic = profiled_traffic()
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "value": value, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
                    "flops_per_step": FLOPS, "l2": "inputs larger than L2 (Q, K, V = 402 MB per step)",
                    "parallelism": "replicas" if world == 1 else f"replicas x{world} (independent batches)"},
@@ -283,23 +328,9 @@ def main():
         "clocks": clk.summary(),
     }
 
-    if not args.no_extras:
+    if args.part == "all":
         line["e2e"] = measure_e2e(torch, ops, q, k, v, args, world, dev)
-        del q, k, v, o, lse
-        torch.cuda.empty_cache()
-        line["combine"] = measure_combine(torch, ops, sc, synth, pk, dev)
-        line["decode_splitk"] = measure_decode(torch, ops, sc, synth, pk, dev)
-        torch.cuda.empty_cache()
-    if rank == 0 and not args.no_cpu_baseline:
-        tf, secs, heads = oracle_sample(12.0)
-        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": f"{heads} whole heads (4096x4096 causal, D=128) of the workload, "
-                                          f"FP64 numpy oracle, {secs:.1f} s"}
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def measure_e2e(torch, ops, q, k, v, args, world, dev):
@@ -358,7 +389,7 @@ def time_launches(torch, fn, iters, flush=None):
     return statistics.median(ts), sum(ts) / len(ts)
 
 
-def measure_combine(torch, ops, sc, synth, pk, dev):
+def measure_combine(torch, ops, sc, synth, pk, dev, Ps, dtypes):
     rows, heads, depth = 4096, 32, 128
     RH = rows * heads
     l2buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -366,7 +397,9 @@ def measure_combine(torch, ops, sc, synth, pk, dev):
            "unit": "GB/s", "l2": "flushed before every launch (512 MB write)", "results": []}
     best = None
     for dt, esz in (("f32", 4), ("bf16", 2)):
-        for P in (2, 8, 16, 32, 37):
+        if dt not in dtypes:
+            continue
+        for P in Ps:
             op = sc.fill_normal(torch.empty((P, RH, depth), dtype=getattr(torch, {"f32": "float32", "bf16": "bfloat16"}[dt]),
                                             device=dev), 21, synth.STREAM_OPART, dt)
             lp = sc.fill_lse(torch.empty((P, RH), dtype=torch.float32, device=dev), 21)
@@ -391,15 +424,16 @@ def measure_combine(torch, ops, sc, synth, pk, dev):
     return out
 
 
-def measure_decode(torch, ops, sc, synth, pk, dev):
-    Bd, Hd, Nkv, Dd = 64, 32, 32768, 128
+def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps):
+    Hd, Nkv, Dd = 32, 32768, 128
     q = sc.fill_normal(torch.empty((Bd, Hd, 1, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_Q, "bf16")
     k = sc.fill_normal(torch.empty((Bd, Hd, Nkv, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_K, "bf16")
     v = sc.fill_normal(torch.empty((Bd, Hd, Nkv, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_V, "bf16")
     RH = Bd * Hd
-    out = {"workload": "decode: 64 sequences x 1 query, 32 heads, 32768 keys, D=128, bf16; fp32 partials, then combine",
-           "unit": "GB/s", "l2": "K and V (34.4 GB) are far larger than L2", "results": []}
-    for P in (4, 8, 16, 37):
+    out = {"workload": f"decode: {Bd} sequences x 1 query, 32 heads, 32768 keys, D=128, bf16; "
+                       "fp32 partials, then combine",
+           "unit": "GB/s", "l2": "K and V are far larger than L2", "results": []}
+    for P in Ps:
         op = torch.empty((P, RH, Dd), dtype=torch.float32, device=dev)
         lp = torch.empty((P, RH), dtype=torch.float32, device=dev)
         o = torch.empty_like(q)

@@ -92,15 +92,18 @@ cudaError_t launch_attn(const AttnArgs& a, int block_n, bool bf16, cudaStream_t 
   }
 }
 
+// Size, dtype and scale checks first; pointer checks only when there is data to touch
+// (an empty problem may come with null pointers, as empty tensors have).
 oattn_status attn_common_checks(const void* q, const void* k, const void* v, int B, int H, int Nq,
                                 int Nkv, int D, float scale, oattn_dtype dtype) {
-  if (!q || !k || !v) return OATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Nq < 0 || Nkv < 0 || D < 1) return OATTN_ERR_INVALID_ARG;
   if ((long long)B * H > 0x7fffffffLL) return OATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return OATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return OATTN_ERR_INVALID_ARG;
   if (!is16(dtype)) return OATTN_ERR_UNSUPPORTED;
   if (!supported_d(D)) return OATTN_ERR_UNSUPPORTED;
+  if (Nq == 0) return OATTN_OK;
+  if (!q || (Nkv > 0 && (!k || !v))) return OATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return OATTN_ERR_INVALID_ARG;
   if (Nq > (1 << 24) || Nkv > (1 << 24)) return OATTN_ERR_UNSUPPORTED;
   return OATTN_OK;
@@ -148,10 +151,10 @@ oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, f
                          struct CUstream_st* stream) {
   oattn_status s = attn_common_checks(q, k, v, B, H, N, N, D, scale, dtype);
   if (s != OATTN_OK) return s;
-  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4))) return OATTN_ERR_INVALID_ARG;
   if (block_n == 0) block_n = 128;
   if (block_n != 32 && block_n != 64 && block_n != 128) return OATTN_ERR_INVALID_ARG;
   if (N == 0) return OATTN_OK;
+  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4))) return OATTN_ERR_INVALID_ARG;
   cudaError_t e;
   AttnArgs a{};
   a.status = status_ptr(&e);
@@ -159,7 +162,7 @@ oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, f
   const bool bf16 = dtype == OATTN_BF16;
   const int BH = B * H;
   if (!make_map(&a.tm_q, q, bf16, BH, N, D, 128) || !make_map(&a.tm_k, k, bf16, BH, N, D, block_n) ||
-      !make_map(&a.tm_v, v, bf16, BH, N, D, block_n))
+      !make_map(&a.tm_v, v, bf16, BH, N, D, block_n) || !make_map(&a.tm_o, o, bf16, BH, N, D, 128))
     return OATTN_ERR_CUDA;
   a.o = o;
   a.lse = lse;
@@ -206,13 +209,14 @@ oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* 
   oattn_status s = attn_common_checks(q, k, v, B, H, Nq, Nkv, D, scale, dtype);
   if (s != OATTN_OK) return s;
   if (causal && Nq != Nkv) return OATTN_ERR_INVALID_ARG;
-  if (P < 1 || P > 256 || !o_partial || !lse_partial) return OATTN_ERR_INVALID_ARG;
+  if (P < 1 || P > 256) return OATTN_ERR_INVALID_ARG;
   if (partial_dtype != OATTN_F32 && partial_dtype != dtype) return OATTN_ERR_INVALID_ARG;
-  if (!aligned(o_partial, 16) || !aligned(lse_partial, 4)) return OATTN_ERR_INVALID_ARG;
   if (lse && !o) return OATTN_ERR_INVALID_ARG;
-  if (o && (!aligned(o, 16) || (lse && !aligned(lse, 4)))) return OATTN_ERR_INVALID_ARG;
   if (o && !combine_supported(D, partial_dtype)) return OATTN_ERR_UNSUPPORTED;
   if (Nq == 0) return OATTN_OK;
+  if (!o_partial || !lse_partial) return OATTN_ERR_INVALID_ARG;
+  if (!aligned(o_partial, 16) || !aligned(lse_partial, 4)) return OATTN_ERR_INVALID_ARG;
+  if (o && (!aligned(o, 16) || (lse && !aligned(lse, 4)))) return OATTN_ERR_INVALID_ARG;
   cudaError_t e;
   unsigned int* status = status_ptr(&e);
   if (!status) return OATTN_ERR_CUDA;
@@ -237,9 +241,13 @@ oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* 
   } else {
     AttnArgs a{};
     a.status = status;
-    if (!make_map(&a.tm_q, q, bf16, BH, Nq, D, 128) || !make_map(&a.tm_k, k, bf16, BH, Nkv, D, 128) ||
-        !make_map(&a.tm_v, v, bf16, BH, Nkv, D, 128))
+    // With no keys the K/V maps are never read; q stands in as a valid base address.
+    const void* kb = Nkv > 0 ? k : q;
+    const void* vb = Nkv > 0 ? v : q;
+    if (!make_map(&a.tm_q, q, bf16, BH, Nq, D, 128) || !make_map(&a.tm_k, kb, bf16, BH, Nkv, D, 128) ||
+        !make_map(&a.tm_v, vb, bf16, BH, Nkv, D, 128))
       return OATTN_ERR_CUDA;
+    a.tm_o = a.tm_q;  // split mode stores its partials without a tensor map
     a.o = o_partial;
     a.lse = lse_partial;
     a.BH = BH; a.N = Nq; a.Nkv = Nkv; a.D = D;

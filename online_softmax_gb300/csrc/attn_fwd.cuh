@@ -12,12 +12,12 @@
 //
 // How it maps onto one GB300 SM (one CTA per SM: 193 KB of shared memory and all 512
 // TMEM columns at D = 128):
-//   * A CTA owns two 128-row query tiles of one head (or of one head and split-K
-//     partition).  Warps 0-3 and 4-7 are two softmax warpgroups, one per query tile;
+//   * A CTA owns two 128-row query tiles of one head (and one split-K partition in
+//     split mode).  Warps 0-3 and 4-7 are two softmax warpgroups, one per query tile;
 //     thread r of a warpgroup owns row r, which is TMEM lane r, so row max and row sum
-//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs, warps
-//     10-11 only complete the third warpgroup so that setmaxnreg can move registers
-//     from it to the softmax warpgroups (224 per softmax thread).
+//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs; warps 10-11
+//     only complete the third warpgroup so that setmaxnreg can move its registers to
+//     the softmax warpgroups (216 per softmax thread).
 //   * Q tiles are copied once; K and V tiles stream through a ring of shared-memory
 //     slots (K in even, V in odd slots) filled by cp.async.bulk.tensor with the
 //     128/64/32-byte swizzle that matches the tcgen05 shared-memory descriptors.
@@ -33,10 +33,15 @@
 //     commit after S_t(j+1) also covers PV_t(j) (commits track every earlier MMA of the
 //     issuing thread), so when the softmax sees S_t(j+1) it may rescale O_t safely.
 //   * The rescale is lazy: a warp keeps its stale maximum until some row's maximum
-//     grows by more than kTau (2^8), so p <= 256, and only then reloads O from TMEM,
-//     multiplies by alpha and stores it back.  Exact arithmetic is unchanged.
-//   * Causal: query tiles are scheduled longest first, wholly-future key tiles are not
-//     visited, and only tiles crossing the diagonal apply the per-element mask.
+//     grows by more than kTauLazy (2^8), so p <= 256, and only then reloads O from
+//     TMEM, multiplies by alpha and stores it back.  Exact arithmetic is unchanged.
+//   * The epilogue writes o / l into the query tile's own (now free) shared memory in
+//     the swizzled layout of the output tensor map and stores it with one TMA copy per
+//     row chunk (rows past the end are clipped by the copy).  Split-K partials are
+//     stored directly from registers (FP32 or 16-bit).
+//   * CTAs are ordered in groups of kHeadGroup heads: within a group the query-tile
+//     pairs run longest first (causal), and the few heads in flight keep their K/V in
+//     L2 instead of streaming every head's K/V from HBM for every pair.
 //
 // Every wait is bounded (see ptx.cuh); a thread that gives up marks the CTA aborted,
 // everyone leaves its loop, copies and MMAs in flight are drained, TMEM is freed.
@@ -70,11 +75,11 @@ struct AttnCfg {
   static constexpr int COL_S0 = 0, COL_S1 = BN, COL_O0 = 2 * BN, COL_O1 = 2 * BN + D;
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN + 2 * D);
   static constexpr int THREADS = 384;       // 2 softmax warpgroups + 1 copy/MMA warpgroup
-  static constexpr int REGS_LAUNCH = 168;    // 65536 / 384 rounded down to a multiple of 8
-  static constexpr int REGS_SOFTMAX = 224;   // after setmaxnreg.inc
-  static constexpr int REGS_OTHER = 56;      // after setmaxnreg.dec
+  static constexpr int REGS_LAUNCH = 168;   // 65536 / 384 rounded down to a multiple of 8
+  static constexpr int REGS_SOFTMAX = 216;  // after setmaxnreg.inc
+  static constexpr int REGS_OTHER = 72;     // after setmaxnreg.dec
   // Per SM sub-partition: two softmax warps and one other warp share what three warps
-  // had at launch (2*224 + 56 = 3*168).
+  // had at launch (2*216 + 72 = 3*168).
   static_assert(2 * REGS_SOFTMAX + REGS_OTHER <= 3 * REGS_LAUNCH, "register split exceeds the launch pool");
   static_assert(NSLOT >= 4, "need at least two K/V tile pairs in flight");
   static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
@@ -84,54 +89,61 @@ struct AttnCfg {
 
 constexpr float kTauLazy = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kHeadGroup = 8;
 
-// Load NC consecutive TMEM columns of this thread's lane as floats (NC % 16 == 0).
+// Compiler fence: the registers filled by earlier tcgen05.ld are valid only after
+// tcgen05.wait::ld; routing them through this empty asm (placed after the wait) keeps
+// every use behind it.
+__device__ __forceinline__ void reg_fence32(uint32_t* v) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                 "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]),
+                 "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]),
+                 "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t* v) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                 "+r"(v[14]), "+r"(v[15]));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Load NC consecutive TMEM columns of this thread's lane (NC = 16 or a multiple of 32):
+// every load is issued first, then one wait.
 template <int NC>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&x)[NC]) {
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&u)[NC]) {
   if constexpr (NC % 32 == 0) {
 #pragma unroll
-    for (int c = 0; c < NC / 32; ++c) {
-      uint32_t u[32];
-      tmem_ld_x32(taddr + c * 32, u);
-      tmem_wait_ld_x32(u);
+    for (int c = 0; c < NC / 32; ++c) tmem_ld_x32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+    tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[i]);
-    }
+    for (int c = 0; c < NC / 32; ++c) reg_fence32(&u[c * 32]);
   } else {
     static_assert(NC == 16, "16 or a multiple of 32 columns");
-    uint32_t u[16];
     tmem_ld_x16(taddr, u);
-    tmem_wait_ld_x16(u);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(u[i]);
+    tmem_wait_ld();
+    reg_fence16(u);
   }
 }
 
-// Multiply NC TMEM columns of this lane by a (read, scale, write back).
+// Multiply NC TMEM columns of this lane by a (read, scale, write back; the caller
+// waits for the stores).
 template <int NC>
 __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float a) {
   constexpr int W = NC % 32 == 0 ? 32 : 16;
 #pragma unroll
   for (int c = 0; c < NC / W; ++c) {
-    if constexpr (W == 32) {
-      uint32_t u[32];
-      tmem_ld_x32(taddr + c * 32, u);
-      tmem_wait_ld_x32(u);
+    uint32_t u[W];
+    tmem_load_cols<W>(taddr + c * W, u);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
-      tmem_st_x32(taddr + c * 32, u);
-    } else {
-      uint32_t u[16];
-      tmem_ld_x16(taddr, u);
-      tmem_wait_ld_x16(u);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
-      tmem_st_x16(taddr, u);
-    }
+    for (int i = 0; i < W; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
+    if constexpr (W == 32) tmem_st_x32(taddr + c * W, u); else tmem_st_x16(taddr + c * W, u);
   }
 }
 
-// Store 16 or 32 output values of a row: 16-bit (rounded to nearest even) or FP32.
+// Store 16 or 32 output values of a row to global memory: FP32 or 16-bit (RNE).
 template <int NV, bool BF16>
 __device__ __forceinline__ void store_row_chunk(void* dst, const float (&y)[NV], bool f32) {
   if (f32) {
@@ -152,6 +164,15 @@ __device__ __forceinline__ void store_row_chunk(void* dst, const float (&y)[NV],
   }
 }
 
+// Byte offset of 16-byte unit u of row r inside one swizzled row chunk (rows of SW
+// bytes): the XOR of address bits [4, 4+log2(SW/16)) with bits [7, ...), the pattern
+// the TMA copies and the MMA descriptors use (chunk bases are 1024-byte aligned).
+template <int SW>
+__device__ __forceinline__ uint32_t swizzled(uint32_t r, uint32_t u) {
+  const uint32_t off = r * SW + u * 16;
+  return off ^ (((off >> 7) & (SW / 16 - 1)) << 4);
+}
+
 // Wait (once) for ring entry n (K_j at n = 2j, V_j at n = 2j+1); `ready` remembers the
 // highest entry already waited for.
 template <int NSLOT>
@@ -163,49 +184,78 @@ __device__ __forceinline__ bool wait_kv(uint64_t* full, int n, int& ready, volat
   return true;
 }
 
+// Shared-memory descriptors are split into a 32-bit low word (start address >> 4 and
+// leading byte offset >> 4) and a high word (stride byte offset >> 4, the fixed 0b001 and
+// the swizzle mode) that is the same for every operand here.  Consecutive K steps only
+// move the start address, so each MMA costs one 32-bit add on a precomputed low word:
+// the single issuing thread must keep up with 64-cycle MMAs.
+template <class C>
+__device__ __forceinline__ uint32_t desc_hi() {
+  return (uint32_t)(((8 * C::SW) >> 4) & 0x3FFF) | (1u << 14) | (C::SWZ << 29);
+}
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) {
+  return ((uint64_t)hi << 32) | lo;
+}
+
 // S_t = Q_t K_j^T: D/16 MMAs of K = 16 (32 bytes of each operand row), walking the
-// swizzled row chunks.  Descriptors are built per step (no hoisting into registers).
+// swizzled row chunks.
 template <class C, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t q_addr, uint32_t kv_addr, int t, int j,
                                          uint64_t* bar) {
   constexpr uint32_t IDESC = idesc_f16(128, C::BN_, BF16, false);
   constexpr int KPC = C::CH / 16;  // K steps per row chunk
-  const uint32_t k_addr = kv_addr + ((2 * j) % C::NSLOT) * C::KV_BYTES;
+  const uint32_t hi = desc_hi<C>();
+  const uint32_t a0 = desc_lo(q_addr, 16);
+  const uint32_t b0 = desc_lo(kv_addr + ((2 * j) % C::NSLOT) * C::KV_BYTES, 16);
   const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
   tc_fence_after();
-#pragma unroll 1
+#pragma unroll
   for (int kk = 0; kk < C::D_ / 16; ++kk) {
     const uint32_t off = (kk % KPC) * 32;
     const uint32_t c = kk / KPC;
-    const uint64_t a = smem_desc(q_addr + c * C::BM * C::SW + off, 16, 8 * C::SW, C::SWZ);
-    const uint64_t b = smem_desc(k_addr + c * C::BN_ * C::SW + off, 16, 8 * C::SW, C::SWZ);
-    mma_ss(d, a, b, IDESC, kk > 0 ? 1u : 0u);
+    mma_ss(d, desc64(a0 + ((c * C::BM * C::SW + off) >> 4), hi),
+           desc64(b0 + ((c * C::BN_ * C::SW + off) >> 4), hi), IDESC, kk > 0 ? 1u : 0u);
   }
   tc_commit(bar);
 }
 
 // O_t += P_t V_j: BN/16 MMAs of K = 16 keys, P read from TMEM (8 packed columns per
-// step), V read MN-major (16 key rows per step).
+// step), V read MN-major (16 key rows per step; the leading byte offset steps between
+// the 64-column chunks of D).
 template <class C, bool BF16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t kv_addr, int t, int j) {
   constexpr uint32_t IDESC = idesc_f16(128, C::D_, BF16, true);
-  const uint32_t v_addr = kv_addr + ((2 * j + 1) % C::NSLOT) * C::KV_BYTES;
+  const uint32_t hi = desc_hi<C>();
+  const uint32_t b0 = desc_lo(kv_addr + ((2 * j + 1) % C::NSLOT) * C::KV_BYTES, C::BN_ * C::SW);
   const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
   const uint32_t p = tmem + (t ? C::COL_S1 : C::COL_S0);
   tc_fence_after();
-#pragma unroll 1
-  for (int kb = 0; kb < C::BN_ / 16; ++kb) {
-    const uint64_t b = smem_desc(v_addr + kb * 16 * C::SW, C::BN_ * C::SW, 8 * C::SW, C::SWZ);
-    mma_ts(d, p + kb * 8, b, IDESC, (j > 0 || kb > 0) ? 1u : 0u);
-  }
+#pragma unroll
+  for (int kb = 0; kb < C::BN_ / 16; ++kb)
+    mma_ts(d, p + kb * 8, desc64(b0 + ((kb * 16 * C::SW) >> 4), hi), IDESC, (j > 0 || kb > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 template <int D, int BN, bool BF16>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
-                    float* __restrict__ lse_out, int BH, int N, int Nkv, int causal, float scale_log2,
-                    int P, int chunk, int out_f32, unsigned int* status) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    void* __restrict__ out, float* __restrict__ lse_out, int BH, int N, int Nkv, int causal,
+                    float scale_log2, int P, int chunk, int out_f32, unsigned int* status) {
   using C = AttnCfg<D, BN>;
   constexpr int BM = C::BM;
   constexpr int NSLOT = C::NSLOT;
@@ -218,7 +268,6 @@ __global__ void __launch_bounds__(384, 1)
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
-  uint8_t* sQ[2] = {smem, smem + C::Q_BYTES};
   uint8_t* sKV = smem + 2 * C::Q_BYTES;
 
   const int tid = threadIdx.x;
@@ -232,24 +281,25 @@ __global__ void __launch_bounds__(384, 1)
   long long idx = blockIdx.x;
   const int part = (int)(idx % nparts);
   idx /= nparts;
-  const int bh = (int)(idx % BH);
-  const int pair_rank = (int)(idx / BH);
+  const int group = (int)(idx / ((long long)kHeadGroup * npairs));
+  const int gheads = min(kHeadGroup, BH - group * kHeadGroup);
+  const int within = (int)(idx - (long long)group * kHeadGroup * npairs);
+  const int pair_rank = within / gheads;
+  const int bh = group * kHeadGroup + within % gheads;
   const int pair = causal ? (npairs - 1 - pair_rank) : pair_rank;
   const int kv_lo = split ? min(part * chunk, Nkv) : 0;
   const int kv_hi = split ? min(kv_lo + chunk, Nkv) : Nkv;
 
-  int row0[2], nkv[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    row0[t] = pair * 2 * BM + t * BM;
-    nkv[t] = 0;
-    if (row0[t] < N) {
-      const int last_row = min(row0[t] + BM - 1, N - 1);
-      const int key_end = causal ? min(kv_hi, last_row + 1) : kv_hi;
-      nkv[t] = key_end > kv_lo ? (key_end - kv_lo + BN - 1) / BN : 0;
-    }
-  }
-  const int nkv_max = max(nkv[0], nkv[1]);
+  // Key tiles needed by the query tile starting at row0; 0 if the tile is empty.
+  auto tiles_for = [&](int row0) -> int {
+    if (row0 >= N) return 0;
+    const int last_row = min(row0 + BM - 1, N - 1);
+    const int key_end = causal ? min(kv_hi, last_row + 1) : kv_hi;
+    return key_end > kv_lo ? (key_end - kv_lo + BN - 1) / BN : 0;
+  };
+  const int row0_0 = pair * 2 * BM, row0_1 = row0_0 + BM;
+  const int nkv0 = tiles_for(row0_0), nkv1 = tiles_for(row0_1);
+  const int nkv_max = max(nkv0, nkv1);
 
   // ---- set-up: barriers, TMEM
   if (warp == 9) {
@@ -281,17 +331,15 @@ __global__ void __launch_bounds__(384, 1)
   // setmaxnreg sits at the top of its role's branch so that the register allocator
   // sees the new limit for all of that role's code.
   if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER));
-  if (warp == 8) {
-    // ================================================================ TMA producer
-    if (lane == 0 && nkv_max > 0) {
-      uint32_t qbytes = 0;
-      for (int t = 0; t < 2; ++t) qbytes += nkv[t] > 0 ? C::Q_BYTES : 0;
-      mbar_arrive_expect_tx(&bar_q, qbytes);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER));
+    if (warp == 8 && lane == 0 && nkv_max > 0) {
+      // ============================================================== TMA producer
+      mbar_arrive_expect_tx(&bar_q, (nkv0 > 0 ? C::Q_BYTES : 0) + (nkv1 > 0 ? C::Q_BYTES : 0));
       for (int t = 0; t < 2; ++t)
-        if (nkv[t] > 0)
+        if ((t ? nkv1 : nkv0) > 0)
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sQ[t] + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, row0[t], bh);
+            tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? row0_1 : row0_0,
+                        bh);
       int issued = 0;
       for (int n = 0; n < 2 * nkv_max; ++n) {
         const int slot = n % NSLOT;
@@ -308,31 +356,34 @@ __global__ void __launch_bounds__(384, 1)
       mbar_drain(&bar_q, 0, status);
       for (int n = max(0, issued - NSLOT); n < issued; ++n)
         mbar_drain(&bar_full[n % NSLOT], (uint32_t)(n / NSLOT) & 1u, status);
-    }
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
-    if (lane == 0 && nkv_max > 0) {
+    } else if (warp == 9 && lane == 0 && nkv_max > 0) {
+      // ============================================================== MMA issuer
+      const uint32_t q_addr0 = smem_u32(smem), q_addr1 = q_addr0 + C::Q_BYTES;
+      const uint32_t kv_addr = smem_u32(sKV);
       bool ok = mbar_wait(&bar_q, 0, abort, status, kErrWaitFull);
       int k_ready = -1, v_ready = -1;
-      if (ok) {
-        for (int t = 0; t < 2 && ok; ++t)
-          if (nkv[t] > 0) {
-            ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
-            if (ok) issue_qk<C, BF16>(tmem, smem_u32(sQ[t]), smem_u32(sKV), t, 0, &bar_s[t]);
-          }
-        if (ok) tc_commit(&bar_empty[0]);  // K_0 is free once both S(0) are done
+      if (ok && nkv0 > 0) {
+        ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
+        if (ok) issue_qk<C, BF16>(tmem, q_addr0, kv_addr, 0, 0, &bar_s[0]);
       }
+      if (ok && nkv1 > 0) {
+        ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
+        if (ok) issue_qk<C, BF16>(tmem, q_addr1, kv_addr, 1, 0, &bar_s[1]);
+      }
+      if (ok) tc_commit(&bar_empty[0]);  // K_0 is free once both S(0) are done
       for (int j = 0; ok && j < nkv_max; ++j) {
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nkv[t]) continue;
+        for (int t = 0; t < 2; ++t) {
+          const int nkv_t = t ? nkv1 : nkv0;
+          if (j >= nkv_t) continue;
           ok = wait_kv<NSLOT>(bar_full, 2 * j + 1, v_ready, abort, status) &&
                mbar_wait(&bar_p[t], (uint32_t)j & 1u, abort, status, kErrWaitP);
           if (!ok) break;
-          issue_pv<C, BF16>(tmem, smem_u32(sKV), t, j);
-          if (j == nkv[t] - 1) tc_commit(&bar_o[t]);
-          if (j + 1 < nkv[t]) {
+          issue_pv<C, BF16>(tmem, kv_addr, t, j);
+          if (j == nkv_t - 1) tc_commit(&bar_o[t]);
+          if (j + 1 < nkv_t) {
             ok = wait_kv<NSLOT>(bar_full, 2 * (j + 1), k_ready, abort, status);
-            if (ok) issue_qk<C, BF16>(tmem, smem_u32(sQ[t]), smem_u32(sKV), t, j + 1, &bar_s[t]);
+            if (!ok) break;
+            issue_qk<C, BF16>(tmem, t ? q_addr1 : q_addr0, kv_addr, t, j + 1, &bar_s[t]);
           }
         }
         if (!ok) break;
@@ -343,14 +394,16 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(&bar_done);
       mbar_drain(&bar_done, 0, status);
     }
-  }  // warps 10-11: nothing to do
+    // warps 10-11 and the other lanes: nothing to do
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX));
     // ================================================================ softmax warpgroups
-    const int t = warp >> 2;   // query tile of this warpgroup
-    const int quad = warp & 3; // TMEM lane quadrant = rows 32*quad .. 32*quad+31
+    const int t = warp >> 2;    // query tile of this warpgroup
+    const int quad = warp & 3;  // TMEM lane quadrant = rows 32*quad .. 32*quad+31
     const int r = quad * 32 + lane;
-    const int row = row0[t] + r;
+    const int row0 = t ? row0_1 : row0_0;
+    const int nkv = t ? nkv1 : nkv0;
+    const int row = row0 + r;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t col_s = t ? C::COL_S1 : C::COL_S0;
     const uint32_t col_o = t ? C::COL_O1 : C::COL_O0;
@@ -358,18 +411,20 @@ __global__ void __launch_bounds__(384, 1)
     float l = 0.f;
     bool ok = true;
 
-    if (row0[t] < N) {
-      for (int j = 0; j < nkv[t]; ++j) {
+    if (row0 < N) {
+      for (int j = 0; j < nkv; ++j) {
         ok = mbar_wait(&bar_s[t], (uint32_t)j & 1u, abort, status, kErrWaitS);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        uint32_t u[BN];
+        tmem_load_cols<BN>(trow + col_s, u);
         float s[BN];
-        tmem_load_cols<BN>(trow + col_s, s);
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
 
         const int key0 = kv_lo + j * BN;
-        const bool need_mask = (key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0[t]);
-        if (need_mask) {
+        if ((key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0)) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) {
             const int key = key0 + c;
@@ -377,20 +432,24 @@ __global__ void __launch_bounds__(384, 1)
             s[c] = vis ? s[c] : -INFINITY;
           }
         }
-        float mx = s[0];
+        // row max as a tree over 8 independent chains
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < BN; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float mnew = fmaxf(m, mx * scale_log2);
         const bool grow = (mnew - m) > kTauLazy;  // false for -inf - -inf (NaN)
         const bool rescale = __any_sync(0xffffffffu, grow);
         const float m_use = rescale ? mnew : m;
         const float alpha = (m_use == m) ? 1.f : ex2(m - m_use);  // ex2(-inf) = 0
-        if (rescale && j > 0) {
-          tmem_scale_cols<D>(trow + col_o, alpha);
-          tmem_wait_st();
-        }
+        if (rescale && j > 0) tmem_scale_cols<D>(trow + col_o, alpha);
         const float base = (m_use == -INFINITY) ? 0.f : m_use;
-        float rowsum = 0.f;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c2 = 0; c2 < BN / 32; ++c2) {
           uint32_t pk[16];
@@ -398,48 +457,83 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 16; ++i) {
             const float p0 = ex2(fmaf(s[c2 * 32 + 2 * i], scale_log2, -base));
             const float p1 = ex2(fmaf(s[c2 * 32 + 2 * i + 1], scale_log2, -base));
-            rowsum += p0 + p1;
+            sum4[i & 3] += p0 + p1;
             pk[i] = pack2<BF16>(p0, p1);
           }
           tmem_st_x16(trow + col_s + c2 * 16, pk);
         }
         tmem_wait_st();
-        l = fmaf(alpha, l, rowsum);
+        l = fmaf(alpha, l, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
         m = m_use;
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
       }
 
       // ---- epilogue: o / l and the log-sum-exp of the row
-      if (ok && nkv[t] > 0) {
+      if (ok && nkv > 0) {
         ok = mbar_wait(&bar_o[t], 0, abort, status, kErrWaitO);
         ok = __all_sync(0xffffffffu, ok);
       }
-      if (ok) {
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        const bool f32 = split && out_f32;
-        const size_t plane = split ? (size_t)part * BH * N : 0;
-        const size_t grow_idx = plane + (size_t)bh * N + row;
-        const size_t esz = f32 ? 4 : 2;
-        uint8_t* dst = static_cast<uint8_t*>(out) + grow_idx * D * esz;
-        constexpr int W = D % 32 == 0 ? 32 : 16;
-        if (nkv[t] > 0) tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      constexpr int W = D % 32 == 0 ? 32 : 16;
+      if (ok && nkv > 0) tc_fence_after();
+      if (!split) {
+        // o / l -> 16-bit -> this tile's Q buffer (free now: the last S_t finished before
+        // the last PV_t) in the output map's swizzled layout -> TMA store.  Every warp of
+        // the warpgroup reaches the barrier, aborted or not; the store is skipped when
+        // the CTA aborted.
+        uint8_t* tile = smem + t * C::Q_BYTES;
+        if (ok) {
 #pragma unroll
-        for (int c = 0; c < D / W; ++c) {
-          float y[W];
-          if (nkv[t] > 0) {
-            tmem_load_cols<W>(trow + col_o + c * W, y);
+          for (int c = 0; c < D / W; ++c) {
+            uint32_t u[W];
+            tmem_load_cols<W>(trow + col_o + c * W, u);
+            uint32_t w[W / 2];
 #pragma unroll
-            for (int i = 0; i < W; ++i) y[i] = y[i] * inv + 0.f;
-          } else {
+            for (int i = 0; i < W / 2; ++i)
+              w[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv + 0.f, __uint_as_float(u[2 * i + 1]) * inv + 0.f);
 #pragma unroll
-            for (int i = 0; i < W; ++i) y[i] = 0.f;
+            for (int v16 = 0; v16 < W / 8; ++v16) {
+              const int col = c * W + v16 * 8;  // first element of this 16-byte unit
+              const int ch = col / C::CH;
+              const int unit = (col % C::CH) / 8;
+              *reinterpret_cast<uint4*>(tile + ch * BM * C::SW + swizzled<C::SW>(r, unit)) =
+                  make_uint4(w[4 * v16], w[4 * v16 + 1], w[4 * v16 + 2], w[4 * v16 + 3]);
+            }
           }
-          if (row < N) store_row_chunk<W, BF16>(dst + (size_t)c * W * esz, y, f32);
+          fence_proxy_async_smem();
         }
-        if (row < N && lse_out != nullptr) {
+        named_bar_sync(1 + t, 128);
+        if (r == 0 && *abort == 0) {
+          for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, tile + c * BM * C::SW, c * C::CH, row0, bh);
+          bulk_commit_group();
+          bulk_wait_group_0();
+        }
+        if (ok && row < N && lse_out != nullptr) {
           const float lse2 = (l > 0.f) ? m + lg2(l) : -INFINITY;
-          lse_out[grow_idx] = split ? lse2 : lse2 * kLn2;
+          lse_out[(size_t)bh * N + row] = lse2 * kLn2;
+        }
+      } else if (ok) {
+        {
+          const bool f32 = out_f32 != 0;
+          const size_t grow_idx = (size_t)part * BH * N + (size_t)bh * N + row;
+          const size_t esz = f32 ? 4 : 2;
+          uint8_t* dst = static_cast<uint8_t*>(out) + grow_idx * D * esz;
+#pragma unroll
+          for (int c = 0; c < D / W; ++c) {
+            float y[W];
+            if (nkv > 0) {
+              uint32_t u[W];
+              tmem_load_cols<W>(trow + col_o + c * W, u);
+#pragma unroll
+              for (int i = 0; i < W; ++i) y[i] = __uint_as_float(u[i]) * inv + 0.f;
+            } else {
+#pragma unroll
+              for (int i = 0; i < W; ++i) y[i] = 0.f;
+            }
+            if (row < N) store_row_chunk<W, BF16>(dst + (size_t)c * W * esz, y, f32);
+          }
+          if (row < N && lse_out != nullptr) lse_out[grow_idx] = (l > 0.f) ? m + lg2(l) : -INFINITY;
         }
       }
     }
@@ -474,8 +568,8 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   const long long blocks = npairs * a.BH * (a.P > 0 ? a.P : 1);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.BH, a.N,
-                                                           a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.BH,
+                                                           a.N, a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
                                                            a.out_f32, a.status);
   return cudaGetLastError();
 }

@@ -32,6 +32,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 // ---- tcgen05 attention forward / split-K partitions (attn_fwd_d*.cu)
 struct AttnArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [BH, N, D], boxes of 128 or BN rows
+  CUtensorMap tm_o;              // plain mode: output map (box of 128 rows); split: unused
   void* o;            // plain: [BH, N, D] dtype;  split: [P, BH*N, D] partial dtype
   float* lse;         // plain: [BH, N] natural log (nullable);  split: [P, BH*N] base 2
   int BH, N, Nkv, D;

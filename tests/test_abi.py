@@ -115,5 +115,11 @@ def test_combine_rejects(lib, kw, expect):
     assert combine(lib, **kw) == expect
 
 
+def test_empty_problems_accept_null_pointers(lib):
+    # N == 0 is a no-op that touches nothing, so null pointers (empty tensors) are fine
+    assert attn(lib, q=None, k=None, v=None, o=None, N=0) == 0
+    assert splitk(lib, q=None, k=None, v=None, op=None, lp=None, Nq=0) == 0
+
+
 def test_device_error_needs_pointer(lib):
     assert lib.oattn_device_error(None) == 1
