@@ -432,38 +432,41 @@ __global__ void __launch_bounds__(384, 1)
             s[c] = vis ? s[c] : -INFINITY;
           }
         }
-        // row max as a tree over 8 independent chains
+        // row max: 8 independent chains of three-input max
         float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = s[i];
 #pragma unroll
-        for (int c = 8; c < BN; c += 8)
+        for (int c = 8; c < BN; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         const float mnew = fmaxf(m, mx * scale_log2);
         const bool grow = (mnew - m) > kTauLazy;  // false for -inf - -inf (NaN)
         const bool rescale = __any_sync(0xffffffffu, grow);
         const float m_use = rescale ? mnew : m;
         const float alpha = (m_use == m) ? 1.f : ex2(m - m_use);  // ex2(-inf) = 0
         if (rescale && j > 0) tmem_scale_cols<D>(trow + col_o, alpha);
-        const float base = (m_use == -INFINITY) ? 0.f : m_use;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float nbase = (m_use == -INFINITY) ? 0.f : -m_use;
+        // p = 2^(s*scale*log2e - m): the scale-and-shift runs on pairs (f32x2 FMA), the
+        // exponential on the MUFU, the row sum on pairs (f32x2 add) over four chains.
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c2 = 0; c2 < BN / 32; ++c2) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(s[c2 * 32 + 2 * i], scale_log2, -base));
-            const float p1 = ex2(fmaf(s[c2 * 32 + 2 * i + 1], scale_log2, -base));
-            sum4[i & 3] += p0 + p1;
+            float x0, x1;
+            ffma2(x0, x1, s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], p0, p1);
             pk[i] = pack2<BF16>(p0, p1);
           }
           tmem_st_x16(trow + col_s + c2 * 16, pk);
         }
         tmem_wait_st();
-        l = fmaf(alpha, l, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+        const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        l = fmaf(alpha, l, rowsum);
         m = m_use;
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
