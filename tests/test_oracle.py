@@ -301,3 +301,38 @@ def test_partition_with_no_visible_key():
     assert np.all(lsep[1, :4] == -np.inf)
     assert np.all(Op[1, :4] == float(g["output"])) and not np.any(np.signbit(Op[1, :4]))
     assert np.all(np.isfinite(lsep[1, 4:]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_rows_brute_force(causal):
+    """Sampled rows (used for the full-size checks) against pure-Python loops."""
+    rng = np.random.default_rng(29)
+    n, d = 11, 3
+    q, k, v = (rng.normal(size=(n, d)) for _ in range(3))
+    rows = np.array([0, 4, 10])
+    O, lse = oracle.attention_rows(q[rows], rows, k, v, 0.7, causal)
+    Ob, lb = _brute_attention(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
+    np.testing.assert_allclose(O, Ob[rows], atol=1e-12)
+    np.testing.assert_allclose(lse, lb[rows], atol=1e-12)
+
+
+def test_splitk_partials_rows_brute_force():
+    """Per-partition outputs and base-2 LSEs against pure-Python loops over each range."""
+    rng = np.random.default_rng(31)
+    n, d = 9, 2
+    q, k, v = (rng.normal(size=(n, d)) for _ in range(3))
+    rows = np.array([1, 5, 8])
+    bounds = [(0, 4), (4, 8), (8, 9), (9, 9)]
+    Op, lp = oracle.splitk_partials_rows(q[rows], rows, k, v, 1.0, True, bounds)
+    for p, (lo, hi) in enumerate(bounds):
+        for ri, i in enumerate(rows):
+            s = [(j, float(q[i] @ k[j])) for j in range(lo, hi) if j <= i]
+            if not s:
+                assert lp[p, ri] == -math.inf and np.all(Op[p, ri] == 0.0)
+                continue
+            m = max(x for _, x in s)
+            w = [(j, math.exp(x - m)) for j, x in s]
+            L = math.fsum(x for _, x in w)
+            assert lp[p, ri] == pytest.approx((m + math.log(L)) / math.log(2.0), abs=1e-12)
+            for dd in range(d):
+                assert Op[p, ri, dd] == pytest.approx(math.fsum(x * v[j][dd] for j, x in w) / L, abs=1e-12)
