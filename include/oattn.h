@@ -122,6 +122,29 @@ oattn_status splitk_combine(const void* o_partial, const float* lse_partial, voi
                             oattn_dtype in_dtype, oattn_dtype out_dtype,
                             struct CUstream_st* stream);
 
+/*
+ * attn_fwd_splitk_noalloc - attn_fwd_splitk for callers that cannot allocate device
+ * memory (for example a plugin whose host framework owns all device memory through its
+ * own pool, or a latency-critical caller that cannot afford the device synchronisation
+ * an allocation may cause).  The reference pages have no counterpart for this entry
+ * point; it only changes where the partition workspace lives.
+ *
+ *   Arguments as attn_fwd_splitk, without o_partial / lse_partial / partial_dtype: the
+ *   float32 partials go to a fixed workspace inside the library (a device array of
+ *   10 Mi + 256 Ki floats, 41 MiB, held on every GPU that loads the library until the
+ *   process exits).  o is required; lse may be NULL.
+ *   Requires P * B*H*Nq * D <= 10485760 and P * B*H*Nq <= 262144, else returns
+ *   OATTN_ERR_UNSUPPORTED before touching the device.  Other errors as attn_fwd_splitk.
+ *   The first call on a device looks up the workspace's device address (a host-side
+ *   runtime call); make that first call before any stream capture.
+ *   Every call uses the same workspace: calls that may overlap on the GPU (different
+ *   streams, or different host threads on one device) race and must be serialised by
+ *   the caller.  Each call rewrites every partial it reads, so no clearing is needed.
+ */
+oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     int B, int H, int Nq, int Nkv, int D, int causal, float scale,
+                                     oattn_dtype dtype, int P, struct CUstream_st* stream);
+
 /* Key chunk per partition used by attn_fwd_splitk (host-only, no GPU needed). */
 int splitk_chunk(int Nkv, int P);
 

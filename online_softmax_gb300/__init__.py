@@ -11,7 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "splitk_combine", "splitk_chunk",
+__all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine", "splitk_chunk",
            "device_error", "OattnError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,13 +37,14 @@ def _load():
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.attn_fwd_bn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     L.attn_fwd_splitk.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i, vp]
+    L.attn_fwd_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
     L.splitk_combine.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
     L.splitk_chunk.argtypes = [i, i]
     L.oattn_status_string.argtypes = [i]
     L.oattn_status_string.restype = ctypes.c_char_p
     L.oattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
-    for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "splitk_combine", "splitk_chunk",
-                 "oattn_device_error"):
+    for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine",
+                 "splitk_chunk", "oattn_device_error"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -150,6 +151,22 @@ def attn_fwd_splitk(q, k, v, P, o_partial, lse_partial, o=None, lse=None, causal
                              _ptr(lse_partial), _dtype_code(o_partial.dtype), _stream(stream))
     _raise(st, "attn_fwd_splitk")
     return o_partial, lse_partial, o, lse
+
+
+def attn_fwd_splitk_noalloc(q, k, v, P, o, lse=None, causal=False, scale=None, stream=None):
+    """Split-K attention without caller-provided workspace: the float32 partials live in
+    a fixed device array inside the library (for callers that cannot allocate device
+    memory).  Calls that overlap on the GPU share that array and race."""
+    import torch
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    _check(q, "q"); _check(k, "k", q.dtype, (B, H, Nkv, D)); _check(v, "v", q.dtype, (B, H, Nkv, D))
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, Nq))
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = lib.attn_fwd_splitk_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nkv, D,
+                                     int(bool(causal)), scale, _dtype_code(q.dtype), int(P), _stream(stream))
+    _raise(st, "attn_fwd_splitk_noalloc")
+    return o, lse
 
 
 def splitk_combine(o_partial, lse_partial, o, lse_out=None, rows=None, heads=1, stream=None):
