@@ -7,11 +7,13 @@
 // registers (lane l keeps partitions l, l+32, ...; five xor shuffles for the max and
 // five for the sum); each partition's scale is then broadcast from its owning lane
 // with one indexed shuffle, and the depth vector of the next partition step is loaded
-// (128-bit loads) before the current one is folded in.  When a partition row is
+// (128-bit loads) before the current one is folded in; the first steps are requested
+// before the LSE reduction, whose loads they do not depend on.  When a partition row is
 // shorter than a warp of 128-bit vectors (16-bit data, depth 128), the warp splits into
 // 32/LPP groups that take consecutive partitions and are summed at the end.  Ladder
-// sizes P in {2, 4, 8, 16, 32} get fully unrolled instances; any other P runs the
-// runtime-bound loop.
+// sizes P in {2, 4, 8, 16, 32} get fully unrolled instances (P <= 4 with four
+// row-heads per warp, all their loads in flight at once); any other P runs the
+// runtime-bound loop, streaming four steps ahead.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -34,9 +36,9 @@ template <> struct Vec<float> { static constexpr int E = 4; };
 template <> struct Vec<__nv_bfloat16> { static constexpr int E = 8; };
 template <> struct Vec<__half> { static constexpr int E = 8; };
 
+// Widen one raw 16-byte vector of T to floats.
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, float (&x)[Vec<T>::E]) {
-  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+__device__ __forceinline__ void widen_vec(const uint4 u, float (&x)[Vec<T>::E]) {
   if constexpr (Vec<T>::E == 4) {
     x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
     x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
@@ -89,6 +91,45 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   const long long rh = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   if (rh >= RH) return;  // whole warp leaves together
 
+  const int sub = lane / LPP;  // which partition of a step this lane folds
+  const int li = lane % LPP;
+  const TIn* base = o_partial + rh * DEPTH + li * E;
+  const long long pstride = RH * (long long)DEPTH;
+  const int steps = (P + PPS - 1) / PPS;
+
+  // Raw 16-byte vectors of step `step` (partition step*PPS + sub); zeros past the last
+  // partition.  They stay packed until folded, which halves the registers that the
+  // prefetch buffers need for 16-bit inputs.
+  auto fetch = [&](int step, uint4 (&x)[VPL]) {
+    const int p = step * PPS + sub;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+      x[v] = (p < P) ? __ldcs(reinterpret_cast<const uint4*>(base + p * pstride + v * LPP * E))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  };
+  float acc[VPL][E];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
+  auto fold = [&](float sc, const uint4 (&x)[VPL]) {
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      float w[E];
+      widen_vec<TIn>(x[v], w);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[v][e] = fmaf(sc, (sc != 0.f) ? w[e] : 0.f, acc[v][e]);
+    }
+  };
+
+  // The partition vectors do not depend on the LSE reduction: the first ones are
+  // requested before it, so both memory latencies overlap.
+  constexpr int STATIC_STEPS = P_STATIC > 0 ? (P_STATIC + PPS - 1) / PPS : 0;
+  constexpr int AHEAD = STATIC_STEPS > 0 ? (STATIC_STEPS <= 8 ? STATIC_STEPS : 2) : 4;
+  uint4 pre[AHEAD][VPL];
+#pragma unroll
+  for (int i = 0; i < AHEAD; ++i) fetch(i, pre[i]);
+
   // ---- LSE reduction, once, into per-lane registers
   float lse[SLOTS];
   float m = -INFINITY;
@@ -111,72 +152,58 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s) lse[s] = dead ? 0.f : ex2(lse[s] - G);  // now scale_p
 
-  // ---- weighted accumulation with the next step's vectors prefetched
-  const int sub = lane / LPP;  // which partition of the step this lane folds
-  const int li = lane % LPP;
-  float acc[VPL][E];
-#pragma unroll
-  for (int v = 0; v < VPL; ++v)
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
-
-  const TIn* base = o_partial + rh * DEPTH + li * E;
-  const long long pstride = RH * (long long)DEPTH;
-  const int steps = (P + PPS - 1) / PPS;
-
-  float cur[VPL][E], nxt[VPL][E];
-  auto fetch = [&](int step, float (&x)[VPL][E]) {
-    const int p = step * PPS + sub;
-    if (p < P) {
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) load_vec<TIn>(base + p * pstride + v * LPP * E, x[v]);
-    } else {
-#pragma unroll
-      for (int v = 0; v < VPL; ++v)
-#pragma unroll
-        for (int e = 0; e < E; ++e) x[v][e] = 0.f;
-    }
-  };
-  auto fold = [&](float sc, float (&x)[VPL][E]) {
-#pragma unroll
-    for (int v = 0; v < VPL; ++v)
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[v][e] = fmaf(sc, (sc != 0.f) ? x[v][e] : 0.f, acc[v][e]);
-  };
-
-  fetch(0, cur);
+  // ---- weighted accumulation
   if constexpr (P_STATIC > 0) {
+    if constexpr (STATIC_STEPS <= 8) {
+      // everything is already in flight: fold in order
 #pragma unroll
-    for (int step = 0; step < (P_STATIC + PPS - 1) / PPS; ++step) {
-      const int p = step * PPS + sub;
-      const float sc = __shfl_sync(0xffffffffu, lse[(step * PPS) / 32], p & 31);
-      if (step + 1 < steps) fetch(step + 1, nxt);
-      fold(p < P ? sc : 0.f, cur);
+      for (int step = 0; step < STATIC_STEPS; ++step) {
+        const int p = step * PPS + sub;
+        const float sc = __shfl_sync(0xffffffffu, lse[(step * PPS) / 32], p & 31);
+        fold(p < P ? sc : 0.f, pre[step]);
+      }
+    } else {
+      // two steps ahead through a register ring (indices are compile-time after unrolling)
 #pragma unroll
-      for (int v = 0; v < VPL; ++v)
+      for (int step = 0; step < STATIC_STEPS; ++step) {
+        const int p = step * PPS + sub;
+        const float sc = __shfl_sync(0xffffffffu, lse[(step * PPS) / 32], p & 31);
+        uint4 cur[VPL];
 #pragma unroll
-        for (int e = 0; e < E; ++e) cur[v][e] = nxt[v][e];
+        for (int v = 0; v < VPL; ++v) cur[v] = pre[step % AHEAD][v];
+        if (step + AHEAD < STATIC_STEPS) fetch(step + AHEAD, pre[step % AHEAD]);
+        fold(p < P ? sc : 0.f, cur);
+      }
     }
   } else {
     // Runtime P: a partition's scale would need a run-time register index, so the
-    // warp parks its per-lane scales in its own shared-memory row instead and every
-    // lane reads the one it needs (a broadcast read).
+    // warp parks its per-lane scales in its own shared-memory row and every lane reads
+    // the one it needs (a broadcast read).  Vectors stream in chunks of four steps,
+    // the next chunk requested before the current one is folded.
     __shared__ float s_scale[kCombineWarps][kMaxP];
     float* my = s_scale[threadIdx.x >> 5];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s)
       if (s * 32 + lane < P) my[s * 32 + lane] = lse[s];
     __syncwarp();
-#pragma unroll 1
-    for (int step = 0; step < steps; ++step) {
-      const int p = step * PPS + sub;
-      const float sc = p < P ? my[p] : 0.f;
-      if (step + 1 < steps) fetch(step + 1, nxt);
-      fold(sc, cur);
+    uint4 nxt[AHEAD][VPL];
+    for (int c0 = 0; c0 < steps; c0 += 2 * AHEAD) {
+      // pre holds steps c0 .. c0+3; request c0+4 .. c0+7 into nxt
 #pragma unroll
-      for (int v = 0; v < VPL; ++v)
+      for (int i = 0; i < AHEAD; ++i) fetch(c0 + AHEAD + i, nxt[i]);
 #pragma unroll
-        for (int e = 0; e < E; ++e) cur[v][e] = nxt[v][e];
+      for (int i = 0; i < AHEAD; ++i) {
+        const int p = (c0 + i) * PPS + sub;
+        fold(p < P ? my[p] : 0.f, pre[i]);
+      }
+      // request c0+8 .. c0+11 into pre, fold nxt
+#pragma unroll
+      for (int i = 0; i < AHEAD; ++i) fetch(c0 + 2 * AHEAD + i, pre[i]);
+#pragma unroll
+      for (int i = 0; i < AHEAD; ++i) {
+        const int p = (c0 + AHEAD + i) * PPS + sub;
+        fold(p < P ? my[p] : 0.f, nxt[i]);
+      }
     }
   }
 
@@ -201,6 +228,97 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   if (lse_out != nullptr && lane == 0) lse_out[rh] = dead ? -INFINITY : G * lse_scale;
 }
 
+// Small P (a ladder rung of at most 4 partitions): a warp owns RPW row-heads and puts
+// every load of all of them in flight before reducing any, so that the few bytes per
+// row-head do not leave the warp waiting on one dependent load chain after another.
+template <typename TIn, typename TOut, int LPP, int VPL, int P_STATIC, int RPW>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    splitk_combine_small_kernel(const TIn* __restrict__ o_partial, const float* __restrict__ lse_partial,
+                                TOut* __restrict__ out, float* __restrict__ lse_out, long long RH,
+                                float lse_scale) {
+  constexpr int E = Vec<TIn>::E;
+  constexpr int PPS = 32 / LPP;
+  constexpr int DEPTH = LPP * VPL * E;
+  constexpr int STEPS = (P_STATIC + PPS - 1) / PPS;
+  static_assert(P_STATIC <= 32, "one LSE per lane");
+  const int lane = threadIdx.x & 31;
+  const long long rh0 = ((long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5)) * RPW;
+  if (rh0 >= RH) return;  // whole warp leaves together
+  const int sub = lane / LPP;
+  const int li = lane % LPP;
+  const long long pstride = RH * (long long)DEPTH;
+
+  uint4 x[RPW][STEPS][VPL];
+  float lse[RPW];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const long long rh = rh0 + r;
+    const bool valid = rh < RH;
+    const TIn* base = o_partial + rh * DEPTH + li * E;
+#pragma unroll
+    for (int st = 0; st < STEPS; ++st) {
+      const int p = st * PPS + sub;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+        x[r][st][v] = (valid && p < P_STATIC)
+                          ? __ldcs(reinterpret_cast<const uint4*>(base + p * pstride + v * LPP * E))
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+    lse[r] = (valid && lane < P_STATIC) ? __ldg(lse_partial + (long long)lane * RH + rh) : -INFINITY;
+  }
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const long long rh = rh0 + r;
+    float m = lse[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const bool dead = (m == -INFINITY);
+    const float msafe = dead ? 0.f : m;
+    float sum = ex2(lse[r] - msafe);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float G = dead ? -INFINITY : lg2(sum) + msafe;
+    const float scale = dead ? 0.f : ex2(lse[r] - G);
+    float acc[VPL][E];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
+#pragma unroll
+    for (int st = 0; st < STEPS; ++st) {
+      const int p = st * PPS + sub;
+      float sc = __shfl_sync(0xffffffffu, scale, p & 31);
+      sc = p < P_STATIC ? sc : 0.f;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        float w[E];
+        widen_vec<TIn>(x[r][st][v], w);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[v][e] = fmaf(sc, (sc != 0.f) ? w[e] : 0.f, acc[v][e]);
+      }
+    }
+#pragma unroll
+    for (int o = LPP; o < 32; o <<= 1)
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[v][e] += __shfl_xor_sync(0xffffffffu, acc[v][e], o);
+    if (rh < RH) {
+      if (sub == 0) {
+        TOut* dst = out + rh * DEPTH + li * E;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          float y[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) y[e] = dead ? 0.f : acc[v][e] + 0.f;
+          store_vec<TOut, E>(dst + v * LPP * E, y);
+        }
+      }
+      if (lse_out != nullptr && lane == 0) lse_out[rh] = dead ? -INFINITY : G * lse_scale;
+    }
+  }
+}
+
 template <typename TIn, typename TOut, int LPP, int VPL>
 cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
                      float lse_scale, cudaStream_t st) {
@@ -208,9 +326,11 @@ cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P,
   const dim3 block(kCombineWarps * 32);
   auto* a = static_cast<const TIn*>(op);
   auto* c = static_cast<TOut*>(o);
+  constexpr int RPW = 4;
+  const dim3 grid_small((unsigned)((RH + kCombineWarps * RPW - 1) / (kCombineWarps * RPW)));
   switch (P) {
-    case 2: splitk_combine_kernel<TIn, TOut, LPP, VPL, 2><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
-    case 4: splitk_combine_kernel<TIn, TOut, LPP, VPL, 4><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    case 2: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, RPW><<<grid_small, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
+    case 4: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, RPW><<<grid_small, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
     case 8: splitk_combine_kernel<TIn, TOut, LPP, VPL, 8><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
     case 16: splitk_combine_kernel<TIn, TOut, LPP, VPL, 16><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
     case 32: splitk_combine_kernel<TIn, TOut, LPP, VPL, 32><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;

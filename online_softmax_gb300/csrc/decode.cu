@@ -8,7 +8,8 @@
 // bandwidth, so it stays off the tensor cores.
 //
 // Per key tile every warp scores its own 8 keys (lane l holds D/32 elements of q and
-// of each key row; five xor shuffles finish each dot product), the four warps agree on
+// of each key row; a butterfly reduce-scatter finishes the 8 dot products with 9
+// shuffles and leaves key k's score in lanes 4k..4k+3), the four warps agree on
 // the tile maximum through the single-barrier cross-warp exchange ("fa4_ws_exchange4"),
 // and then all warps update the running maximum identically.  Because that maximum is
 // bit-identical in every warp, each warp can keep its own partial denominator and
@@ -40,7 +41,7 @@ namespace {
 
 constexpr int kTK = 32;          // keys per stage
 constexpr int kKeysPerWarp = 8;  // kTK / 4 warps
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr int kThreads = 160;    // 4 compute warps + 1 copy warp
 constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
 
@@ -148,23 +149,46 @@ __global__ void __launch_bounds__(kThreads)
       const uint16_t* vs = sm.v[s];
       const int key0 = t * kTK + warp * kKeysPerWarp;  // first key of this warp, partition-relative
 
-      float sc[kKeysPerWarp];
-      float tmax = -INFINITY;
+      // Partial dot products of this lane's EPL elements with the warp's 8 keys.
+      float dp[kKeysPerWarp];
 #pragma unroll
       for (int i = 0; i < kKeysPerWarp; ++i) {
-        float part_dot = 0.f;
-        const bool valid = ok && key0 + i < nkeys;  // warp-uniform
-        if (valid && lane < LANES) {
+        dp[i] = 0.f;
+        if (ok && lane < LANES) {  // rows past the partition end hold stale data: masked below
           float kf[EPL];
           load_row<EPL, BF16>(ks + (warp * kKeysPerWarp + i) * D + lane * EPL, kf);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) part_dot = fmaf(qv[e], kf[e], part_dot);
+          for (int e = 0; e < EPL; ++e) dp[i] = fmaf(qv[e], kf[e], dp[i]);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part_dot += __shfl_xor_sync(0xffffffffu, part_dot, off);
-        sc[i] = valid ? part_dot * scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, sc[i]);
       }
+      // Butterfly reduce-scatter: after the xor-16/8/4 halving steps and two xor
+      // reductions, lanes 4k..4k+3 hold the full dot product of key k (9 shuffles for 8
+      // keys instead of 5 per key).
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+      float e4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float send = b4 ? dp[j] : dp[j + 4];
+        const float keep = b4 ? dp[j + 4] : dp[j];
+        e4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+      float f2[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float send = b3 ? e4[j] : e4[j + 2];
+        const float keep = b3 ? e4[j + 2] : e4[j];
+        f2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+      float g = (b2 ? f2[1] : f2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? f2[0] : f2[1], 4);
+      g += __shfl_xor_sync(0xffffffffu, g, 2);
+      g += __shfl_xor_sync(0xffffffffu, g, 1);
+      const int my_key = (lane >> 2) & 7;  // key of this lane's score within the warp's 8
+      const bool valid = ok && key0 + my_key < nkeys;
+      const float sc = valid ? g * scale_log2 : -INFINITY;
+      float tmax = sc;  // max over the 8 keys (lanes of one key agree)
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
       // All four warps agree on the tile maximum (bit-identical result everywhere).
       tmax = ws_exchange<4, 32, true>(tmax, lane, warp, 0, seq++, sm.xchg, 1);
       const float mnew = fmaxf(m, tmax);
@@ -176,17 +200,22 @@ __global__ void __launch_bounds__(kThreads)
         m = mnew;
       }
       const float base = (m == -INFINITY) ? 0.f : m;
+      const float pk = ex2(sc - base);  // 0 for masked keys
+      // Sum over the 8 keys: the xor-4/8/16 partners hold the 8 different keys, so each
+      // key is counted once in every lane.
+      float psum = pk;
+      psum += __shfl_xor_sync(0xffffffffu, psum, 4);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 8);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 16);
+      l += psum;
 #pragma unroll
       for (int i = 0; i < kKeysPerWarp; ++i) {
-        if (ok && key0 + i < nkeys) {  // warp-uniform: skip rows the copy did not fill
-          const float p = ex2(sc[i] - base);
-          l += p;
-          if (lane < LANES) {
-            float vf[EPL];
-            load_row<EPL, BF16>(vs + (warp * kKeysPerWarp + i) * D + lane * EPL, vf);
+        const float p = __shfl_sync(0xffffffffu, pk, 4 * i);
+        if (ok && key0 + i < nkeys && lane < LANES) {  // warp-uniform except the lane test
+          float vf[EPL];
+          load_row<EPL, BF16>(vs + (warp * kKeysPerWarp + i) * D + lane * EPL, vf);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[e] = fmaf(p, vf[e], o[e]);
-          }
+          for (int e = 0; e < EPL; ++e) o[e] = fmaf(p, vf[e], o[e]);
         }
       }
       __syncwarp();
