@@ -11,8 +11,8 @@
 // before the LSE reduction, whose loads they do not depend on.  When a partition row is
 // shorter than a warp of 128-bit vectors (16-bit data, depth 128), the warp splits into
 // 32/LPP groups that take consecutive partitions and are summed at the end.  Ladder
-// sizes P in {2, 4, 8, 16, 32} get fully unrolled instances (P <= 4 with four
-// row-heads per warp, all their loads in flight at once); any other P runs the
+// sizes P in {2, 4, 8, 16, 32} get fully unrolled instances (P <= 4 with eight or
+// four row-heads per warp, all their loads in flight at once); any other P runs the
 // runtime-bound loop, streaming four steps ahead.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -269,14 +269,18 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     const long long rh = rh0 + r;
+    // Only lanes 0..P-1 hold an LSE: reduce over that many lanes, then broadcast.
+    constexpr int W = P_STATIC <= 1 ? 1 : (P_STATIC <= 2 ? 2 : (P_STATIC <= 4 ? 4 : 32));
     float m = lse[r];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = W / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    m = __shfl_sync(0xffffffffu, m, 0);
     const bool dead = (m == -INFINITY);
     const float msafe = dead ? 0.f : m;
     float sum = ex2(lse[r] - msafe);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = W / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    sum = __shfl_sync(0xffffffffu, sum, 0);
     const float G = dead ? -INFINITY : lg2(sum) + msafe;
     const float scale = dead ? 0.f : ex2(lse[r] - G);
     float acc[VPL][E];
@@ -326,11 +330,12 @@ cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P,
   const dim3 block(kCombineWarps * 32);
   auto* a = static_cast<const TIn*>(op);
   auto* c = static_cast<TOut*>(o);
-  constexpr int RPW = 4;
-  const dim3 grid_small((unsigned)((RH + kCombineWarps * RPW - 1) / (kCombineWarps * RPW)));
+  // row-heads per warp: 8 at P = 2, 4 at P = 4 (the prefetch buffers grow with P)
+  const dim3 grid_small8((unsigned)((RH + kCombineWarps * 8 - 1) / (kCombineWarps * 8)));
+  const dim3 grid_small4((unsigned)((RH + kCombineWarps * 4 - 1) / (kCombineWarps * 4)));
   switch (P) {
-    case 2: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, RPW><<<grid_small, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
-    case 4: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, RPW><<<grid_small, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
+    case 2: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, 8><<<grid_small8, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
+    case 4: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, 4><<<grid_small4, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
     case 8: splitk_combine_kernel<TIn, TOut, LPP, VPL, 8><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
     case 16: splitk_combine_kernel<TIn, TOut, LPP, VPL, 16><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
     case 32: splitk_combine_kernel<TIn, TOut, LPP, VPL, 32><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
