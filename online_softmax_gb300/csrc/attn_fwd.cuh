@@ -216,8 +216,8 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t q_addr, uint32_
   for (int kk = 0; kk < C::D_ / 16; ++kk) {
     const uint32_t off = (kk % KPC) * 32;
     const uint32_t c = kk / KPC;
-    mma_ss(d, desc64(a0 + ((c * C::BM * C::SW + off) >> 4), hi),
-           desc64(b0 + ((c * C::BN_ * C::SW + off) >> 4), hi), IDESC, kk > 0 ? 1u : 0u);
+    mma_ss_lo(d, a0 + ((c * C::BM * C::SW + off) >> 4), b0 + ((c * C::BN_ * C::SW + off) >> 4), hi, IDESC,
+              kk > 0 ? 1u : 0u);
   }
   tc_commit(bar);
 }
@@ -235,7 +235,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t kv_addr, int t,
   tc_fence_after();
 #pragma unroll
   for (int kb = 0; kb < C::BN_ / 16; ++kb)
-    mma_ts(d, p + kb * 8, desc64(b0 + ((kb * 16 * C::SW) >> 4), hi), IDESC, (j > 0 || kb > 0) ? 1u : 0u);
+    mma_ts_lo(d, p + kb * 8, b0 + ((kb * 16 * C::SW) >> 4), hi, IDESC, (j > 0 || kb > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
