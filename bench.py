@@ -330,7 +330,23 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
 
     if args.part == "all":
         line["e2e"] = measure_e2e(torch, ops, q, k, v, args, world, dev)
+        line["context"] = measure_sdpa(torch, q, k, v)
     return line
+
+
+def measure_sdpa(torch, q, k, v):
+    """torch.nn.functional.scaled_dot_product_attention (PyTorch's own backend choice) on
+    the same inputs: a comparison point reported beside the result, not a baseline."""
+    import torch.nn.functional as F
+    fn = lambda: F.scaled_dot_product_attention(q, k, v, is_causal=CAUSAL)
+    try:
+        for _ in range(3):
+            fn()
+        med, _ = time_launches(torch, fn, 20)
+    except RuntimeError as e:  # a backend may be unavailable on this build
+        return {"sdpa": f"unavailable: {str(e).splitlines()[0][:120]}"}
+    return {"sdpa_tflops": FLOPS / med / 1e12, "sdpa_ms": med * 1e3,
+            "note": "torch SDPA, default backend selection, same inputs; context only"}
 
 
 def measure_e2e(torch, ops, q, k, v, args, world, dev):
@@ -439,12 +455,19 @@ def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps):
         op = torch.empty((P, RH, Dd), dtype=torch.float32, device=dev)
         lp = torch.empty((P, RH), dtype=torch.float32, device=dev)
         o = torch.empty_like(q)
+        # attn_fwd_splitk with an output: the combine is a programmatic dependent launch
         fn = lambda: ops.attn_fwd_splitk(q, k, v, P, op, lp, o, None)
+        # the same two kernels as two separate calls (plain stream order)
+        fn_sep = lambda: (ops.attn_fwd_splitk(q, k, v, P, op, lp, None, None),
+                          ops.splitk_combine(op, lp, o.view(RH, Dd), rows=Bd, heads=Hd))
         fn()
+        fn_sep()
         med, _ = time_launches(torch, fn, 10)
+        med_sep, _ = time_launches(torch, fn_sep, 10)
         nbytes = 2 * Bd * Hd * Nkv * Dd * 2 + q.numel() * 2 + 2 * (P * RH * Dd * 4 + P * RH * 4) + o.numel() * 2
         gbs = nbytes / med / 1e9
-        out["results"].append({"P": P, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"]})
+        out["results"].append({"P": P, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"],
+                               "us_separate_calls": med_sep * 1e6, "pdl_speedup": med_sep / med})
     assert ops.device_error() == 0
     fr = [r["frac"] for r in out["results"]]
     out["roofline"] = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "frac_min": min(fr),

@@ -196,7 +196,7 @@ oattn_status splitk_combine(const void* o_partial, const float* lse_partial, voi
     return OATTN_ERR_INVALID_ARG;
   if (!combine_supported(depth, in_dtype)) return OATTN_ERR_UNSUPPORTED;
   const long long RH = (long long)rows * heads;
-  return launch_combine(o_partial, lse_partial, o, lse_out, P, RH, depth, in_dtype, out_dtype, 1.0f,
+  return launch_combine(o_partial, lse_partial, o, lse_out, P, RH, depth, in_dtype, out_dtype, 1.0f, false,
                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? OATTN_OK
              : OATTN_ERR_CUDA;
@@ -260,8 +260,9 @@ oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* 
   }
   if (le != cudaSuccess) return OATTN_ERR_CUDA;
   if (o) {
+    // The combine is a programmatic dependent of the producer just launched on this stream.
     le = launch_combine(o_partial, lse_partial, o, lse, P, (long long)BH * Nq, D, partial_dtype, dtype,
-                        kLn2f, st);
+                        kLn2f, true, st);
     if (le != cudaSuccess) return OATTN_ERR_CUDA;
   }
   return OATTN_OK;

@@ -28,6 +28,32 @@ namespace oattn {
 namespace {
 
 constexpr int kCombineWarps = 8;  // row-heads per 256-thread block
+
+// Programmatic dependent launch ("fa4_splitk_combine", PDL paragraph): when the combine
+// is launched as a dependent of the split-K producer, its blocks may start while the
+// producer's last blocks are still running; every thread waits here, before its first
+// read, until the producer grid has completed and its writes are visible.  The
+// producer issues no early trigger, so the release is its completion.  Without a
+// programmatic dependency the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kern` with the programmatic-stream-serialisation attribute when pdl is set.
+template <typename Kern, typename... Args>
+cudaError_t launch_maybe_pdl(bool pdl, Kern kern, dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 constexpr int kMaxP = 256;
 constexpr int kLseSlots = kMaxP / 32;
 
@@ -87,6 +113,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   constexpr int SLOTS = P_STATIC > 0 ? (P_STATIC + 31) / 32 : kLseSlots;
   const int P = P_STATIC > 0 ? P_STATIC : P_rt;
 
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const long long rh = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   if (rh >= RH) return;  // whole warp leaves together
@@ -241,6 +268,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   constexpr int DEPTH = LPP * VPL * E;
   constexpr int STEPS = (P_STATIC + PPS - 1) / PPS;
   static_assert(P_STATIC <= 32, "one LSE per lane");
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const long long rh0 = ((long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5)) * RPW;
   if (rh0 >= RH) return;  // whole warp leaves together
@@ -325,7 +353,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 
 template <typename TIn, typename TOut, int LPP, int VPL>
 cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
-                     float lse_scale, cudaStream_t st) {
+                     float lse_scale, bool pdl, cudaStream_t st) {
   const dim3 grid((unsigned)((RH + kCombineWarps - 1) / kCombineWarps));
   const dim3 block(kCombineWarps * 32);
   auto* a = static_cast<const TIn*>(op);
@@ -333,40 +361,41 @@ cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P,
   // row-heads per warp: 8 at P = 2, 4 at P = 4 (the prefetch buffers grow with P)
   const dim3 grid_small8((unsigned)((RH + kCombineWarps * 8 - 1) / (kCombineWarps * 8)));
   const dim3 grid_small4((unsigned)((RH + kCombineWarps * 4 - 1) / (kCombineWarps * 4)));
+  cudaError_t e;
   switch (P) {
-    case 2: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, 8><<<grid_small8, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
-    case 4: splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, 4><<<grid_small4, block, 0, st>>>(a, lp, c, lo, RH, lse_scale); break;
-    case 8: splitk_combine_kernel<TIn, TOut, LPP, VPL, 8><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
-    case 16: splitk_combine_kernel<TIn, TOut, LPP, VPL, 16><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
-    case 32: splitk_combine_kernel<TIn, TOut, LPP, VPL, 32><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
-    default: splitk_combine_kernel<TIn, TOut, LPP, VPL, 0><<<grid, block, 0, st>>>(a, lp, c, lo, P, RH, lse_scale); break;
+    case 2: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, 8>, grid_small8, block, st, a, lp, c, lo, RH, lse_scale); break;
+    case 4: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, 4>, grid_small4, block, st, a, lp, c, lo, RH, lse_scale); break;
+    case 8: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 8>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+    case 16: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 16>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+    case 32: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 32>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+    default: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 0>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename TIn, typename TOut>
 cudaError_t launch_depth(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
-                         int depth, float lse_scale, cudaStream_t st) {
+                         int depth, float lse_scale, bool pdl, cudaStream_t st) {
   constexpr int E = Vec<TIn>::E;
   const int nvec = depth / E;  // 16-byte vectors per partition row
   switch (nvec) {
-    case 2: return launch_p<TIn, TOut, 2, 1>(op, lp, o, lo, P, RH, lse_scale, st);
-    case 4: return launch_p<TIn, TOut, 4, 1>(op, lp, o, lo, P, RH, lse_scale, st);
-    case 8: return launch_p<TIn, TOut, 8, 1>(op, lp, o, lo, P, RH, lse_scale, st);
-    case 16: return launch_p<TIn, TOut, 16, 1>(op, lp, o, lo, P, RH, lse_scale, st);
-    case 32: return launch_p<TIn, TOut, 32, 1>(op, lp, o, lo, P, RH, lse_scale, st);
-    case 64: return launch_p<TIn, TOut, 32, 2>(op, lp, o, lo, P, RH, lse_scale, st);
+    case 2: return launch_p<TIn, TOut, 2, 1>(op, lp, o, lo, P, RH, lse_scale, pdl, st);
+    case 4: return launch_p<TIn, TOut, 4, 1>(op, lp, o, lo, P, RH, lse_scale, pdl, st);
+    case 8: return launch_p<TIn, TOut, 8, 1>(op, lp, o, lo, P, RH, lse_scale, pdl, st);
+    case 16: return launch_p<TIn, TOut, 16, 1>(op, lp, o, lo, P, RH, lse_scale, pdl, st);
+    case 32: return launch_p<TIn, TOut, 32, 1>(op, lp, o, lo, P, RH, lse_scale, pdl, st);
+    case 64: return launch_p<TIn, TOut, 32, 2>(op, lp, o, lo, P, RH, lse_scale, pdl, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename TIn>
 cudaError_t launch_out(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
-                       int depth, int out_dt, float lse_scale, cudaStream_t st) {
+                       int depth, int out_dt, float lse_scale, bool pdl, cudaStream_t st) {
   switch (out_dt) {
-    case kF32: return launch_depth<TIn, float>(op, lp, o, lo, P, RH, depth, lse_scale, st);
-    case kBF16: return launch_depth<TIn, __nv_bfloat16>(op, lp, o, lo, P, RH, depth, lse_scale, st);
-    case kF16: return launch_depth<TIn, __half>(op, lp, o, lo, P, RH, depth, lse_scale, st);
+    case kF32: return launch_depth<TIn, float>(op, lp, o, lo, P, RH, depth, lse_scale, pdl, st);
+    case kBF16: return launch_depth<TIn, __nv_bfloat16>(op, lp, o, lo, P, RH, depth, lse_scale, pdl, st);
+    case kF16: return launch_depth<TIn, __half>(op, lp, o, lo, P, RH, depth, lse_scale, pdl, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -381,13 +410,13 @@ bool combine_supported(int depth, int in_dt) {
 }
 
 cudaError_t launch_combine(const void* o_partial, const float* lse_partial, void* o, float* lse_out,
-                           int P, long long RH, int depth, int in_dt, int out_dt, float lse_scale,
+                           int P, long long RH, int depth, int in_dt, int out_dt, float lse_scale, bool pdl,
                            cudaStream_t st) {
   if (RH <= 0) return cudaSuccess;
   switch (in_dt) {
-    case kF32: return launch_out<float>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, st);
-    case kBF16: return launch_out<__nv_bfloat16>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, st);
-    case kF16: return launch_out<__half>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, st);
+    case kF32: return launch_out<float>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, pdl, st);
+    case kBF16: return launch_out<__nv_bfloat16>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, pdl, st);
+    case kF16: return launch_out<__half>(o_partial, lse_partial, o, lse_out, P, RH, depth, out_dt, lse_scale, pdl, st);
     default: return cudaErrorInvalidValue;
   }
 }

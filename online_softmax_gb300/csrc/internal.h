@@ -9,9 +9,11 @@ enum DType : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
 
 // ---- splitk_combine (combine.cu)
 bool combine_supported(int depth, int in_dt);
+// pdl: launch as a programmatic dependent of the previous kernel on the stream (the
+// combine's blocks wait for that grid's completion before their first read).
 cudaError_t launch_combine(const void* o_partial, const float* lse_partial, void* o,
                            float* lse_out, int P, long long RH, int depth, int in_dt, int out_dt,
-                           float lse_scale, cudaStream_t st);
+                           float lse_scale, bool pdl, cudaStream_t st);
 
 // ---- one-query split-K decode on CUDA cores (decode.cu)
 struct DecodeArgs {
