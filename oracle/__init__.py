@@ -12,7 +12,9 @@ Pages it restates (by title and section):
     state (m, l) with empty state (-inf, 0), m' = max(m, rowmax x),
     alpha = exp(m - m'), p = exp(x - m'), l' = alpha*l + rowsum p, numerator
     o' = alpha*o + p V, normalise after the last tile, fully masked rows give
-    output 0 and log-sum-exp -inf.
+    output 0 and log-sum-exp -inf.  Section "Attention as a consumer": the
+    worked kernel takes an optional Boolean M x N mask (here True = visible,
+    combined with the causal and bounds rules).
   * "A3. Tiled attention with online normalization", sections "Keep three
     quantities for each query row" (the recurrence, softmax(QK^T/sqrt(D)) V) and
     "Masks that preserve the recurrence" (causal keeps key <= query).
@@ -30,6 +32,9 @@ notes):
     lse_p = -inf;
   * in the combine a partition whose lse_p is -inf contributes nothing; a row
     whose every lse_p is -inf gives O = +0 and G = -inf.
+  * the optional mask may hide every key of a row (the workshop page leaves that
+    policy to the caller); such a row takes the fully-masked convention of the
+    online statistics: O = +0, LSE = -inf.
 
 Every function below is pinned by tests under ``tests/test_oracle.py`` against
 values the pages print (the worked trace, the two-zeros update), closed forms
@@ -140,14 +145,20 @@ def masked_softmax_attention(s: np.ndarray, vis: np.ndarray, v: np.ndarray):
     return O + 0.0, M, L
 
 
-def attention(q, k, v, scale: float, causal: bool):
+def attention(q, k, v, scale: float, causal: bool, mask=None):
     """Scaled dot-product attention for one head or a batch of heads.
 
     q [..., Nq, D], k [..., Nk, D], v [..., Nk, Dv], all float64 holding the
     exact input values.  Returns O [..., Nq, Dv] and natural-log
     LSE [..., Nq] (= M + ln L; -inf for a row with no visible key).
     Causal requires Nq == Nk ("Masks that preserve the recurrence": rectangular
-    causal lengths are rejected)."""
+    causal lengths are rejected).
+
+    mask: optional Boolean [Nq, Nk] (shared by every head) or [..., Nq, Nk] (one per
+    head), True = the key is visible ("Streaming attention and online state",
+    Attention as a consumer: an optional Boolean M x N mask).  It is combined with the
+    causal rule; a row left with no visible key gives O = +0 and LSE = -inf (Online
+    statistics: entirely masked rows normalise to zero with log-sum-exp -inf)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -161,23 +172,30 @@ def attention(q, k, v, scale: float, causal: bool):
     O = np.empty((qf.shape[0], nq, vf.shape[-1]))
     LSE = np.empty((qf.shape[0], nq))
     vis = visible(nq, nk, causal)
+    if mask is not None:
+        mask = np.asarray(mask, dtype=bool)
+        mask = np.broadcast_to(mask, lead + (nq, nk)).reshape(-1, nq, nk)
     for h in range(qf.shape[0]):
         s = scale * (qf[h] @ kf[h].T)
-        o, M, L = masked_softmax_attention(s, vis, vf[h])
+        vis_h = vis if mask is None else (vis & mask[h])
+        o, M, L = masked_softmax_attention(s, vis_h, vf[h])
         O[h] = o
         LSE[h] = np.where(np.isfinite(M), M + np.log(np.where(L > 0, L, 1.0)), -np.inf)
     return O.reshape(*lead, nq, vf.shape[-1]), LSE.reshape(*lead, nq)
 
 
-def attention_rows(q_rows, rows, k, v, scale: float, causal: bool):
+def attention_rows(q_rows, rows, k, v, scale: float, causal: bool, mask_rows=None):
     """Attention for selected query rows of one head: q_rows [r, D] are the
-    queries at global indices `rows`; k [Nk, D], v [Nk, Dv].  Same definition
+    queries at global indices `rows`; k [Nk, D], v [Nk, Dv]; mask_rows [r, Nk]
+    Boolean or None (the selected rows of the optional mask).  Same definition
     as `attention`, so sampled outputs of a large problem can be checked."""
     q_rows = np.asarray(q_rows, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     s = scale * (q_rows @ k.T)
     vis = visible(len(rows), k.shape[0], causal, q_rows=rows)
+    if mask_rows is not None:
+        vis = vis & np.asarray(mask_rows, dtype=bool)
     O, M, L = masked_softmax_attention(s, vis, v)
     lse = np.where(np.isfinite(M), M + np.log(np.where(L > 0, L, 1.0)), -np.inf)
     return O, lse
@@ -194,9 +212,10 @@ def splitk_bounds(nkv: int, P: int, block_n: int):
     return [(min(p * C, nkv), min((p + 1) * C, nkv)) for p in range(P)]
 
 
-def splitk_partials_rows(q_rows, rows, k, v, scale: float, causal: bool, bounds):
+def splitk_partials_rows(q_rows, rows, k, v, scale: float, causal: bool, bounds, mask_rows=None):
     """Per-partition locally normalised outputs and base-2 LSEs for selected
-    query rows of one head.  Returns O_p [P, r, Dv] and lse_p [P, r] where
+    query rows of one head (mask_rows: [r, Nk] Boolean or None, as in
+    `attention_rows`).  Returns O_p [P, r, Dv] and lse_p [P, r] where
     lse_p = log2(l_p) + m_p with m_p the row max in log2 units, i.e.
     (M_p + ln L_p) * log2(e); an empty (row, partition) gives O_p = 0, lse_p = -inf."""
     q_rows = np.asarray(q_rows, dtype=np.float64)
@@ -207,6 +226,8 @@ def splitk_partials_rows(q_rows, rows, k, v, scale: float, causal: bool, bounds)
     lsep = np.full((len(bounds), len(rows)), -np.inf)
     for p, (lo, hi) in enumerate(bounds):
         vis = visible(len(rows), k.shape[0], causal, q_rows=rows, k_lo=lo, k_hi=hi)
+        if mask_rows is not None:
+            vis = vis & np.asarray(mask_rows, dtype=bool)
         o, M, L = masked_softmax_attention(s, vis, v)
         Op[p] = o
         ok = np.isfinite(M)
@@ -214,8 +235,9 @@ def splitk_partials_rows(q_rows, rows, k, v, scale: float, causal: bool, bounds)
     return Op, lsep
 
 
-def splitk_partials(q, k, v, scale: float, causal: bool, P: int, block_n: int):
-    """Split-K partials for every row of every head: q [..., Nq, D].
+def splitk_partials(q, k, v, scale: float, causal: bool, P: int, block_n: int, mask=None):
+    """Split-K partials for every row of every head: q [..., Nq, D]; mask as in
+    `attention` (Boolean, broadcast against [..., Nq, Nk]) or None.
     Returns O_p [P, ..., Nq, Dv] and lse_p [P, ..., Nq] (base 2)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -230,8 +252,11 @@ def splitk_partials(q, k, v, scale: float, causal: bool, P: int, block_n: int):
     vf = v.reshape(-1, nk, v.shape[-1])
     Op = np.zeros((P, qf.shape[0], nq, vf.shape[-1]))
     lsep = np.full((P, qf.shape[0], nq), -np.inf)
+    if mask is not None:
+        mask = np.broadcast_to(np.asarray(mask, dtype=bool), lead + (nq, nk)).reshape(-1, nq, nk)
     for h in range(qf.shape[0]):
-        o, l = splitk_partials_rows(qf[h], np.arange(nq), kf[h], vf[h], scale, causal, bounds)
+        o, l = splitk_partials_rows(qf[h], np.arange(nq), kf[h], vf[h], scale, causal, bounds,
+                                    None if mask is None else mask[h])
         Op[:, h] = o
         lsep[:, h] = l
     return Op.reshape(P, *lead, nq, vf.shape[-1]), lsep.reshape(P, *lead, nq)

@@ -336,3 +336,88 @@ def test_splitk_partials_rows_brute_force():
             assert lp[p, ri] == pytest.approx((m + math.log(L)) / math.log(2.0), abs=1e-12)
             for dd in range(d):
                 assert Op[p, ri, dd] == pytest.approx(math.fsum(x * v[j][dd] for j, x in w) / L, abs=1e-12)
+
+
+# --- the optional Boolean mask ---------------------------------------------------
+def _brute_masked(q, k, v, scale, causal, mask):
+    nq, nk, dv = len(q), len(k), len(v[0])
+    O, LSE = [], []
+    for i in range(nq):
+        s = [(j, scale * sum(q[i][d] * k[j][d] for d in range(len(q[i]))))
+             for j in range(nk) if mask[i][j] and (not causal or j <= i)]
+        if not s:
+            O.append([0.0] * dv)
+            LSE.append(-math.inf)
+            continue
+        m = max(x for _, x in s)
+        e = [(j, math.exp(x - m)) for j, x in s]
+        L = math.fsum(w for _, w in e)
+        O.append([math.fsum(w * v[j][d] for j, w in e) / L for d in range(dv)])
+        LSE.append(m + math.log(L))
+    return np.array(O), np.array(LSE)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_masked_attention_brute_force(causal):
+    rng = np.random.default_rng(41)
+    n, d = 10, 3
+    q, k, v = (rng.normal(size=(n, d)) for _ in range(3))
+    mask = rng.random((n, n)) < 0.4
+    mask[2, :] = False                      # a fully masked row
+    O, lse = oracle.attention(q, k, v, 0.6, causal, mask=mask)
+    Ob, lb = _brute_masked(q.tolist(), k.tolist(), v.tolist(), 0.6, causal, mask.tolist())
+    np.testing.assert_allclose(O, Ob, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(lb))
+    np.testing.assert_allclose(lse[np.isfinite(lb)], lb[np.isfinite(lb)], atol=1e-12)
+    assert np.all(O[2] == 0.0) and not np.any(np.signbit(O[2])) and lse[2] == -np.inf
+
+
+def test_mask_special_cases_reduce_to_known_rules():
+    rng = np.random.default_rng(43)
+    n, d = 9, 4
+    q, k, v = (rng.normal(size=(2, n, d)) for _ in range(3))
+    O, lse = oracle.attention(q, k, v, 0.5, False)
+    O1, l1 = oracle.attention(q, k, v, 0.5, False, mask=np.ones((n, n), bool))
+    np.testing.assert_array_equal(O1, O)
+    np.testing.assert_array_equal(l1, lse)
+    Oc, lc = oracle.attention(q, k, v, 0.5, True)
+    O2, l2 = oracle.attention(q, k, v, 0.5, False, mask=np.tril(np.ones((n, n), bool)))
+    np.testing.assert_allclose(O2, Oc, atol=1e-14)
+    np.testing.assert_allclose(l2, lc, atol=1e-14)
+    # one mask per head
+    per_head = np.stack([np.tril(np.ones((n, n), bool)), np.ones((n, n), bool)])
+    O3, l3 = oracle.attention(q, k, v, 0.5, False, mask=per_head)
+    np.testing.assert_allclose(O3[0], Oc[0], atol=1e-14)
+    np.testing.assert_allclose(O3[1], O[1], atol=1e-14)
+
+
+def test_masked_splitk_partials_merge_to_masked_attention():
+    """Cutting the key axis commutes with an arbitrary mask: the partitions of a masked
+    problem, merged by the combine, give the masked attention (with rows that a whole
+    partition, or the whole mask, hides)."""
+    rng = np.random.default_rng(47)
+    n, d, P = 12, 4, 3
+    q, k, v = (rng.normal(size=(2, n, d)) for _ in range(3))
+    mask = rng.random((2, n, n)) < 0.5
+    mask[0, 5, :] = False
+    mask[1, 7, :4] = False
+    Op, lsep = oracle.splitk_partials(q, k, v, 0.7, False, P, 4, mask=mask)
+    O, G = oracle.combine(Op.reshape(P, -1, d), lsep.reshape(P, -1))
+    Oa, la = oracle.attention(q, k, v, 0.7, False, mask=mask)
+    np.testing.assert_allclose(O.reshape(2, n, d), Oa, atol=1e-12)
+    la2 = la.reshape(-1) * oracle.LOG2E
+    np.testing.assert_array_equal(np.isneginf(G), np.isneginf(la2))
+    np.testing.assert_allclose(G[np.isfinite(G)], la2[np.isfinite(la2)], atol=1e-12)
+    assert np.isneginf(lsep[:, 0, 5]).all() and np.isneginf(lsep[0, 1, 7])
+
+
+def test_masked_attention_rows_match_full():
+    rng = np.random.default_rng(53)
+    n, d = 11, 3
+    q, k, v = (rng.normal(size=(n, d)) for _ in range(3))
+    mask = rng.random((n, n)) < 0.3
+    O, lse = oracle.attention(q, k, v, 0.9, True, mask=mask)
+    rows = np.array([0, 4, 10])
+    Or, lr = oracle.attention_rows(q[rows], rows, k, v, 0.9, True, mask_rows=mask[rows])
+    np.testing.assert_array_equal(Or, O[rows])
+    np.testing.assert_array_equal(lr, lse[rows])
