@@ -1,7 +1,8 @@
 /*
  * oattn.h - C ABI of the online-softmax attention library for NVIDIA GB300 (sm_103a).
  *
- * Three operations, all asynchronous on the caller's CUDA stream:
+ * Three operations (each also with an optional Boolean mask), all asynchronous on the
+ * caller's CUDA stream:
  *
  *   attn_fwd         single-pass tiled scaled-dot-product attention forward with the
  *                    online-softmax recurrence ("A3. Tiled attention with online
@@ -144,6 +145,65 @@ oattn_status splitk_combine(const void* o_partial, const float* lse_partial, voi
 oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                                      int B, int H, int Nq, int Nkv, int D, int causal, float scale,
                                      oattn_dtype dtype, int P, struct CUstream_st* stream);
+
+/*
+ * The optional Boolean M x N mask ("Streaming attention and online state", section
+ * "Attention as a consumer": the worked attention kernel takes an optional Boolean input
+ * mask of queries by keys).  The kernels read it packed, one bit per key:
+ *
+ *   a packed row holds attn_mask_words(Nkv) = 4*ceil(Nkv/128) 32-bit words; bit j of
+ *   word w (value 1u << j) stands for key 32*w + j and is set when the key is visible.
+ *   Bits at or past Nkv are ignored.  The mask is combined with the causal rule and
+ *   the sequence bounds: a key is used when all three allow it.  A row whose every key
+ *   is hidden gets output +0 and LSE -inf (the fully masked convention of "Streaming
+ *   attention and online state", section "Online statistics").
+ *
+ *   In the masked entry points, row (b, h, q) of the mask starts at
+ *   mask_bits + b*mask_stride_b + h*mask_stride_h + q*mask_stride_q (strides in 32-bit
+ *   words, >= 0, multiples of 4; a stride of 0 shares the rows along that axis, e.g. one
+ *   [N, Nkv] mask for every head, or a key-padding mask [B, Nkv] with mask_stride_h =
+ *   mask_stride_q = 0).  mask_bits is a device pointer on a 16-byte boundary, owned by
+ *   the caller and only read.
+ */
+int attn_mask_words(int Nkv);
+
+/*
+ * attn_mask_pack - pack a byte mask into the bit layout above.
+ *
+ *   mask  device bytes; row r (0 <= r < rows) is mask[r*row_stride .. r*row_stride + Nkv),
+ *         nonzero = visible (a bool tensor's storage).  row_stride >= Nkv, in bytes.
+ *   bits  device words, [rows, attn_mask_words(Nkv)], 16-byte aligned; every word is
+ *         written (bits past Nkv as zero).
+ * rows == 0 or Nkv == 0 is a no-op.  Returns OATTN_ERR_INVALID_ARG for negative sizes,
+ * null or misaligned pointers or row_stride < Nkv.
+ */
+oattn_status attn_mask_pack(const void* mask, unsigned int* bits, long long rows, int Nkv,
+                            long long row_stride, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_masked - attn_fwd (key tiles of 128) with the optional Boolean mask added.
+ *   Arguments as attn_fwd, plus the packed mask and its strides (above); the mask is
+ *   required (non-NULL) when N > 0.  Causal and mask may be combined.
+ */
+oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int D, int causal, float scale,
+                             oattn_dtype dtype, const unsigned int* mask_bits,
+                             long long mask_stride_b, long long mask_stride_h,
+                             long long mask_stride_q, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_splitk_masked - attn_fwd_splitk with the optional Boolean mask (above) over
+ *   the Nq x Nkv scores of each head.  A (row, partition) whose keys are all hidden
+ *   stores O_p = +0 and lse_p = -inf, like an empty partition.  Nq == 1 reads only
+ *   row q = 0 of each (b, h), so mask_stride_q is not used there.
+ */
+oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int H, int Nq, int Nkv, int D,
+                                    int causal, float scale, oattn_dtype dtype, int P,
+                                    void* o_partial, float* lse_partial,
+                                    oattn_dtype partial_dtype, const unsigned int* mask_bits,
+                                    long long mask_stride_b, long long mask_stride_h,
+                                    long long mask_stride_q, struct CUstream_st* stream);
 
 /* Key chunk per partition used by attn_fwd_splitk (host-only, no GPU needed). */
 int splitk_chunk(int Nkv, int P);

@@ -12,6 +12,7 @@ import ctypes
 import os
 
 __all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine", "splitk_chunk",
+           "attn_mask_words", "attn_mask_pack", "attn_fwd_masked", "attn_fwd_splitk_masked",
            "device_error", "OattnError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,11 +41,18 @@ def _load():
     L.attn_fwd_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
     L.splitk_combine.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
     L.splitk_chunk.argtypes = [i, i]
+    ll = ctypes.c_longlong
+    L.attn_mask_words.argtypes = [i]
+    L.attn_mask_pack.argtypes = [vp, vp, ll, i, ll, vp]
+    L.attn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, ll, ll, vp]
+    L.attn_fwd_splitk_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i,
+                                         vp, ll, ll, ll, vp]
     L.oattn_status_string.argtypes = [i]
     L.oattn_status_string.restype = ctypes.c_char_p
     L.oattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine",
-                 "splitk_chunk", "oattn_device_error"):
+                 "splitk_chunk", "oattn_device_error", "attn_mask_words", "attn_mask_pack", "attn_fwd_masked",
+                 "attn_fwd_splitk_masked"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -191,6 +199,97 @@ def splitk_combine(o_partial, lse_partial, o, lse_out=None, rows=None, heads=1, 
                             _dtype_code(o.dtype), _stream(stream))
     _raise(st, "splitk_combine")
     return o, lse_out
+
+
+def attn_mask_words(nkv: int) -> int:
+    """32-bit words per packed mask row: 4 * ceil(nkv / 128)."""
+    return lib.attn_mask_words(int(nkv))
+
+
+def attn_mask_pack(mask, bits=None, stream=None):
+    """Pack a Boolean mask [..., Nq, Nkv] (bool or uint8 CUDA tensor; nonzero = the key is
+    visible) into the bit layout the masked kernels read: int32 [..., Nq, W] with
+    W = attn_mask_words(Nkv), bit j of word w = key 32*w + j.  The rows must be evenly
+    strided: a contiguous tensor, or a 2-D slice [:, :Nkv] of a wider buffer."""
+    import torch
+    if not mask.is_cuda:
+        raise ValueError("mask must be a CUDA tensor")
+    if mask.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("mask must be bool or uint8")
+    if mask.dim() < 2:
+        raise ValueError("mask needs at least two dimensions [..., Nq, Nkv]")
+    nkv = mask.shape[-1]
+    rows = mask.numel() // nkv if nkv else 0
+    if mask.is_contiguous():
+        row_stride = nkv
+    elif mask.dim() == 2 and mask.stride(-1) == 1 and mask.stride(0) >= nkv:
+        row_stride = mask.stride(0)  # rows of a wider buffer
+    else:
+        raise ValueError("mask must be contiguous, or a 2-D slice of rows with a contiguous key axis")
+    W = attn_mask_words(nkv)
+    if bits is None:
+        bits = torch.empty(*mask.shape[:-1], W, dtype=torch.int32, device=mask.device)
+    _check(bits, "bits", torch.int32, tuple(mask.shape[:-1]) + (W,))
+    st = lib.attn_mask_pack(_ptr(mask), _ptr(bits), int(rows), int(nkv), int(row_stride), _stream(stream))
+    _raise(st, "attn_mask_pack")
+    return bits
+
+
+def _mask_strides(bits, B, H, Nq, Nkv, stream):
+    """Packed mask (int32 [..., W]) or Boolean mask (packed here) broadcast against
+    [B, H, Nq, *] -> (tensor kept alive, pointer, stride_b, stride_h, stride_q)."""
+    import torch
+    if bits.dtype in (torch.bool, torch.uint8):
+        bits = attn_mask_pack(bits if bits.is_contiguous() or bits.dim() == 2 else bits.contiguous(), stream=stream)
+    if bits.dtype != torch.int32 or not bits.is_cuda:
+        raise TypeError("mask must be a CUDA bool/uint8 mask or its int32 packed bits")
+    W = attn_mask_words(Nkv)
+    if bits.shape[-1] != W or bits.stride(-1) != 1:
+        raise ValueError(f"packed mask rows must hold {W} contiguous words")
+    while bits.dim() < 4:
+        bits = bits.unsqueeze(0)
+    if stream is not None:
+        bits.record_stream(stream)  # a mask packed here must outlive the launch on `stream`
+    bits = bits.expand(B, H, Nq, W)
+    sb, sh, sq = (bits.stride(0) if B > 1 else 0, bits.stride(1) if H > 1 else 0, bits.stride(2) if Nq > 1 else 0)
+    return bits, _ptr(bits), sb, sh, sq
+
+
+def attn_fwd_masked(q, k, v, o, mask, lse=None, causal=False, scale=None, stream=None):
+    """Attention forward with the optional Boolean mask.  q, k, v, o: [B, H, N, D];
+    mask: Boolean [.., N, N] broadcastable to [B, H, N, N] (True = visible), or its
+    packed bits from attn_mask_pack (int32 [.., N, W])."""
+    import torch
+    B, H, N, D = q.shape
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, q.shape)
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, N))
+    scale = D ** -0.5 if scale is None else float(scale)
+    keep, mp, sb, sh, sq = _mask_strides(mask, B, H, N, N, stream)
+    st = lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, int(bool(causal)),
+                             scale, _dtype_code(q.dtype), mp, sb, sh, sq, _stream(stream))
+    _raise(st, "attn_fwd_masked")
+    return o, lse
+
+
+def attn_fwd_splitk_masked(q, k, v, P, o_partial, lse_partial, mask, o=None, lse=None, causal=False,
+                           scale=None, stream=None):
+    """Split-K attention with the optional Boolean mask [.., Nq, Nkv] (or its packed
+    bits), otherwise as attn_fwd_splitk."""
+    import torch
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    _check(q, "q"); _check(k, "k", q.dtype, (B, H, Nkv, D)); _check(v, "v", q.dtype, (B, H, Nkv, D))
+    _check(o_partial, "o_partial", None, (P, B * H * Nq, D))
+    _check(lse_partial, "lse_partial", torch.float32, (P, B * H * Nq))
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, Nq))
+    scale = D ** -0.5 if scale is None else float(scale)
+    keep, mp, sb, sh, sq = _mask_strides(mask, B, H, Nq, Nkv, stream)
+    st = lib.attn_fwd_splitk_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nkv, D,
+                                    int(bool(causal)), scale, _dtype_code(q.dtype), int(P), _ptr(o_partial),
+                                    _ptr(lse_partial), _dtype_code(o_partial.dtype), mp, sb, sh, sq,
+                                    _stream(stream))
+    _raise(st, "attn_fwd_splitk_masked")
+    return o_partial, lse_partial, o, lse
 
 
 def device_error() -> int:

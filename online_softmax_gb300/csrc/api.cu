@@ -109,6 +109,124 @@ oattn_status attn_common_checks(const void* q, const void* k, const void* v, int
   return OATTN_OK;
 }
 
+// The packed mask: 16-byte aligned words, strides in words that keep every 128-key
+// tile of a row on a 16-byte boundary.
+oattn_status mask_checks(const unsigned int* bits, long long sb, long long sh, long long sq) {
+  if (!bits || !aligned(bits, 16)) return OATTN_ERR_INVALID_ARG;
+  if (sb < 0 || sh < 0 || sq < 0 || sb % 4 || sh % 4 || sq % 4) return OATTN_ERR_INVALID_ARG;
+  return OATTN_OK;
+}
+
+MaskArgs mask_args(const unsigned int* bits, long long sb, long long sh, long long sq, int H) {
+  MaskArgs m{};
+  m.bits = reinterpret_cast<const uint32_t*>(bits);
+  m.sb = sb;
+  m.sh = sh;
+  m.sq = sq;
+  m.H = H;
+  return m;
+}
+
+oattn_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                           int N, int D, int causal, float scale, oattn_dtype dtype, int block_n,
+                           const MaskArgs& mk, cudaStream_t st) {
+  oattn_status s = attn_common_checks(q, k, v, B, H, N, N, D, scale, dtype);
+  if (s != OATTN_OK) return s;
+  if (block_n == 0) block_n = 128;
+  if (block_n != 32 && block_n != 64 && block_n != 128) return OATTN_ERR_INVALID_ARG;
+  if (N == 0) return OATTN_OK;
+  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4))) return OATTN_ERR_INVALID_ARG;
+  cudaError_t e;
+  AttnArgs a{};
+  a.status = status_ptr(&e);
+  if (!a.status) return OATTN_ERR_CUDA;
+  const bool bf16 = dtype == OATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, bf16, BH, N, D, 128) || !make_map(&a.tm_k, k, bf16, BH, N, D, block_n) ||
+      !make_map(&a.tm_v, v, bf16, BH, N, D, block_n) || !make_map(&a.tm_o, o, bf16, BH, N, D, 128))
+    return OATTN_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.Nkv = N;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * kLog2e;
+  a.P = 0;
+  a.chunk = 0;
+  a.out_f32 = 0;
+  a.mask = mk;
+  return launch_attn(a, block_n, bf16, st) == cudaSuccess ? OATTN_OK : OATTN_ERR_CUDA;
+}
+
+oattn_status attn_fwd_splitk_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                  int H, int Nq, int Nkv, int D, int causal, float scale, oattn_dtype dtype,
+                                  int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
+                                  const MaskArgs& mk, cudaStream_t st) {
+  oattn_status s = attn_common_checks(q, k, v, B, H, Nq, Nkv, D, scale, dtype);
+  if (s != OATTN_OK) return s;
+  if (causal && Nq != Nkv) return OATTN_ERR_INVALID_ARG;
+  if (P < 1 || P > 256) return OATTN_ERR_INVALID_ARG;
+  if (partial_dtype != OATTN_F32 && partial_dtype != dtype) return OATTN_ERR_INVALID_ARG;
+  if (lse && !o) return OATTN_ERR_INVALID_ARG;
+  if (o && !combine_supported(D, partial_dtype)) return OATTN_ERR_UNSUPPORTED;
+  if (Nq == 0) return OATTN_OK;
+  if (!o_partial || !lse_partial) return OATTN_ERR_INVALID_ARG;
+  if (!aligned(o_partial, 16) || !aligned(lse_partial, 4)) return OATTN_ERR_INVALID_ARG;
+  if (o && (!aligned(o, 16) || (lse && !aligned(lse, 4)))) return OATTN_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* status = status_ptr(&e);
+  if (!status) return OATTN_ERR_CUDA;
+  const int BH = B * H;
+  const int chunk = splitk_chunk(Nkv, P);
+  const bool bf16 = dtype == OATTN_BF16;
+  cudaError_t le;
+  if (Nq == 1) {
+    // One query row per head: matrix-vector work, streamed on CUDA cores.  (Causal with
+    // Nq == Nkv == 1 sees its single key, the same as non-causal.)
+    DecodeArgs d{};
+    d.q = q; d.k = k; d.v = v;
+    d.o_partial = o_partial;
+    d.lse_partial = lse_partial;
+    d.BH = BH; d.Nkv = Nkv; d.D = D; d.P = P; d.chunk = chunk;
+    d.scale_log2 = scale * kLog2e;
+    d.dtype = dtype;
+    d.partial_dtype = partial_dtype;
+    d.mask = mk;
+    d.status = status;
+    le = launch_decode(d, st);
+  } else {
+    AttnArgs a{};
+    a.status = status;
+    // With no keys the K/V maps are never read; q stands in as a valid base address.
+    const void* kb = Nkv > 0 ? k : q;
+    const void* vb = Nkv > 0 ? v : q;
+    if (!make_map(&a.tm_q, q, bf16, BH, Nq, D, 128) || !make_map(&a.tm_k, kb, bf16, BH, Nkv, D, 128) ||
+        !make_map(&a.tm_v, vb, bf16, BH, Nkv, D, 128))
+      return OATTN_ERR_CUDA;
+    a.tm_o = a.tm_q;  // split mode stores its partials without a tensor map
+    a.o = o_partial;
+    a.lse = lse_partial;
+    a.BH = BH; a.N = Nq; a.Nkv = Nkv; a.D = D;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * kLog2e;
+    a.P = P;
+    a.chunk = chunk;
+    a.out_f32 = partial_dtype == OATTN_F32 ? 1 : 0;
+    a.mask = mk;
+    le = launch_attn(a, 128, bf16, st);
+  }
+  if (le != cudaSuccess) return OATTN_ERR_CUDA;
+  if (o) {
+    // The combine is a programmatic dependent of the producer just launched on this stream.
+    le = launch_combine(o_partial, lse_partial, o, lse, P, (long long)BH * Nq, D, partial_dtype, dtype,
+                        kLn2f, true, st);
+    if (le != cudaSuccess) return OATTN_ERR_CUDA;
+  }
+  return OATTN_OK;
+}
+
 }  // namespace
 }  // namespace oattn
 
@@ -149,35 +267,8 @@ oattn_status oattn_device_error(int* code) {
 oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int N, int D, int causal, float scale, oattn_dtype dtype, int block_n,
                          struct CUstream_st* stream) {
-  oattn_status s = attn_common_checks(q, k, v, B, H, N, N, D, scale, dtype);
-  if (s != OATTN_OK) return s;
-  if (block_n == 0) block_n = 128;
-  if (block_n != 32 && block_n != 64 && block_n != 128) return OATTN_ERR_INVALID_ARG;
-  if (N == 0) return OATTN_OK;
-  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4))) return OATTN_ERR_INVALID_ARG;
-  cudaError_t e;
-  AttnArgs a{};
-  a.status = status_ptr(&e);
-  if (!a.status) return OATTN_ERR_CUDA;
-  const bool bf16 = dtype == OATTN_BF16;
-  const int BH = B * H;
-  if (!make_map(&a.tm_q, q, bf16, BH, N, D, 128) || !make_map(&a.tm_k, k, bf16, BH, N, D, block_n) ||
-      !make_map(&a.tm_v, v, bf16, BH, N, D, block_n) || !make_map(&a.tm_o, o, bf16, BH, N, D, 128))
-    return OATTN_ERR_CUDA;
-  a.o = o;
-  a.lse = lse;
-  a.BH = BH;
-  a.N = N;
-  a.Nkv = N;
-  a.D = D;
-  a.causal = causal ? 1 : 0;
-  a.scale_log2 = scale * kLog2e;
-  a.P = 0;
-  a.chunk = 0;
-  a.out_f32 = 0;
-  return launch_attn(a, block_n, bf16, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? OATTN_OK
-             : OATTN_ERR_CUDA;
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, block_n, MaskArgs{},
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -206,66 +297,51 @@ oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* 
                              int H, int Nq, int Nkv, int D, int causal, float scale, oattn_dtype dtype,
                              int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
                              struct CUstream_st* stream) {
-  oattn_status s = attn_common_checks(q, k, v, B, H, Nq, Nkv, D, scale, dtype);
-  if (s != OATTN_OK) return s;
-  if (causal && Nq != Nkv) return OATTN_ERR_INVALID_ARG;
-  if (P < 1 || P > 256) return OATTN_ERR_INVALID_ARG;
-  if (partial_dtype != OATTN_F32 && partial_dtype != dtype) return OATTN_ERR_INVALID_ARG;
-  if (lse && !o) return OATTN_ERR_INVALID_ARG;
-  if (o && !combine_supported(D, partial_dtype)) return OATTN_ERR_UNSUPPORTED;
-  if (Nq == 0) return OATTN_OK;
-  if (!o_partial || !lse_partial) return OATTN_ERR_INVALID_ARG;
-  if (!aligned(o_partial, 16) || !aligned(lse_partial, 4)) return OATTN_ERR_INVALID_ARG;
-  if (o && (!aligned(o, 16) || (lse && !aligned(lse, 4)))) return OATTN_ERR_INVALID_ARG;
-  cudaError_t e;
-  unsigned int* status = status_ptr(&e);
-  if (!status) return OATTN_ERR_CUDA;
-  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int BH = B * H;
-  const int chunk = splitk_chunk(Nkv, P);
-  const bool bf16 = dtype == OATTN_BF16;
-  cudaError_t le;
-  if (Nq == 1) {
-    // One query row per head: matrix-vector work, streamed on CUDA cores.  (Causal with
-    // Nq == Nkv == 1 sees its single key, the same as non-causal.)
-    DecodeArgs d{};
-    d.q = q; d.k = k; d.v = v;
-    d.o_partial = o_partial;
-    d.lse_partial = lse_partial;
-    d.BH = BH; d.Nkv = Nkv; d.D = D; d.P = P; d.chunk = chunk;
-    d.scale_log2 = scale * kLog2e;
-    d.dtype = dtype;
-    d.partial_dtype = partial_dtype;
-    d.status = status;
-    le = launch_decode(d, st);
-  } else {
-    AttnArgs a{};
-    a.status = status;
-    // With no keys the K/V maps are never read; q stands in as a valid base address.
-    const void* kb = Nkv > 0 ? k : q;
-    const void* vb = Nkv > 0 ? v : q;
-    if (!make_map(&a.tm_q, q, bf16, BH, Nq, D, 128) || !make_map(&a.tm_k, kb, bf16, BH, Nkv, D, 128) ||
-        !make_map(&a.tm_v, vb, bf16, BH, Nkv, D, 128))
-      return OATTN_ERR_CUDA;
-    a.tm_o = a.tm_q;  // split mode stores its partials without a tensor map
-    a.o = o_partial;
-    a.lse = lse_partial;
-    a.BH = BH; a.N = Nq; a.Nkv = Nkv; a.D = D;
-    a.causal = causal ? 1 : 0;
-    a.scale_log2 = scale * kLog2e;
-    a.P = P;
-    a.chunk = chunk;
-    a.out_f32 = partial_dtype == OATTN_F32 ? 1 : 0;
-    le = launch_attn(a, 128, bf16, st);
+  return attn_fwd_splitk_impl(q, k, v, o, lse, B, H, Nq, Nkv, D, causal, scale, dtype, P, o_partial,
+                              lse_partial, partial_dtype, MaskArgs{}, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_mask_words(int Nkv) { return Nkv < 0 ? 0 : mask_words(Nkv); }
+
+oattn_status attn_mask_pack(const void* mask, unsigned int* bits, long long rows, int Nkv, long long row_stride,
+                            struct CUstream_st* stream) {
+  if (rows < 0 || Nkv < 0) return OATTN_ERR_INVALID_ARG;
+  if (rows == 0 || Nkv == 0) return OATTN_OK;
+  if (!mask || !bits || !aligned(bits, 16) || row_stride < Nkv) return OATTN_ERR_INVALID_ARG;
+  if (rows > (1LL << 40)) return OATTN_ERR_UNSUPPORTED;
+  return launch_mask_pack(static_cast<const uint8_t*>(mask), reinterpret_cast<uint32_t*>(bits), rows, Nkv,
+                          row_stride, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? OATTN_OK
+             : OATTN_ERR_CUDA;
+}
+
+oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int N, int D, int causal, float scale, oattn_dtype dtype,
+                             const unsigned int* mask_bits, long long mask_stride_b, long long mask_stride_h,
+                             long long mask_stride_q, struct CUstream_st* stream) {
+  if (N > 0) {
+    const oattn_status s = mask_checks(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q);
+    if (s != OATTN_OK) return s;
   }
-  if (le != cudaSuccess) return OATTN_ERR_CUDA;
-  if (o) {
-    // The combine is a programmatic dependent of the producer just launched on this stream.
-    le = launch_combine(o_partial, lse_partial, o, lse, P, (long long)BH * Nq, D, partial_dtype, dtype,
-                        kLn2f, true, st);
-    if (le != cudaSuccess) return OATTN_ERR_CUDA;
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, 128,
+                       mask_args(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q, H),
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                    int H, int Nq, int Nkv, int D, int causal, float scale, oattn_dtype dtype,
+                                    int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
+                                    const unsigned int* mask_bits, long long mask_stride_b,
+                                    long long mask_stride_h, long long mask_stride_q,
+                                    struct CUstream_st* stream) {
+  if (Nq > 0 && Nkv > 0) {
+    const oattn_status s = mask_checks(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q);
+    if (s != OATTN_OK) return s;
   }
-  return OATTN_OK;
+  // With no keys every row is empty whatever the mask says: run unmasked.
+  const MaskArgs mk = Nkv > 0 ? mask_args(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q, H) : MaskArgs{};
+  return attn_fwd_splitk_impl(q, k, v, o, lse, B, H, Nq, Nkv, D, causal, scale, dtype, P, o_partial,
+                              lse_partial, partial_dtype, mk, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

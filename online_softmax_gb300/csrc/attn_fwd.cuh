@@ -7,8 +7,9 @@
 // key tiles; each tile gives m' = max(m, rowmax s), alpha = exp(m - m'),
 // p = exp(s - m'), l' = alpha l + rowsum p, o' = alpha o + p V; after the last tile the
 // output is o / l and the row's log-sum-exp is m + log l.  Masked scores (keys past the
-// end, keys after the query when causal, keys outside the split-K partition) are -inf
-// and give p = 0; a row that saw no key ends with l = 0 and stores 0 and -inf.
+// end, keys after the query when causal, keys outside the split-K partition, keys the
+// optional Boolean mask hides) are -inf and give p = 0; a row that saw no key ends
+// with l = 0 and stores 0 and -inf.
 //
 // How it maps onto one GB300 SM (one CTA per SM: 193 KB of shared memory and all 512
 // TMEM columns at D = 128):
@@ -39,6 +40,11 @@
 //     the swizzled layout of the output tensor map and stores it with one TMA copy per
 //     row chunk (rows past the end are clipped by the copy).  Split-K partials are
 //     stored directly from registers (FP32 or 16-bit).
+//   * The optional Boolean M x N mask ("Streaming attention and online state", section
+//     "Attention as a consumer") arrives packed one bit per key: each softmax thread
+//     reads the 16 bytes of its row that cover the key tile while it waits for the
+//     tile's scores, and turns the hidden scores to -inf with selects; a warp whose 32 rows see the whole tile
+//     skips the selects.
 //   * CTAs are ordered in groups of kHeadGroup heads: within a group the query-tile
 //     pairs run longest first (causal), and the few heads in flight keep their K/V in
 //     L2 instead of streaming every head's K/V from HBM for every pair.
@@ -250,12 +256,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int D, int BN, bool BF16>
+// 16 bytes of the packed mask (read-only path; rows of a shared mask stay in L2).
+__device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <int D, int BN, bool BF16, bool MASK>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     void* __restrict__ out, float* __restrict__ lse_out, int BH, int N, int Nkv, int causal,
-                    float scale_log2, int P, int chunk, int out_f32, unsigned int* status) {
+                    float scale_log2, int P, int chunk, int out_f32, const MaskArgs mk, unsigned int* status) {
+  static_assert(!MASK || BN == 128, "the packed mask is read in 128-key tiles");
   using C = AttnCfg<D, BN>;
   constexpr int BM = C::BM;
   constexpr int NSLOT = C::NSLOT;
@@ -410,9 +426,22 @@ __global__ void __launch_bounds__(384, 1)
     float m = -INFINITY;  // running max in use, log2 units of scale*s
     float l = 0.f;
     bool ok = true;
+    // This row's packed mask words from the partition's first key; tile j's 16 bytes
+    // are loaded before the wait for S_t(j), so the load overlaps the wait.
+    const uint32_t* mrow = nullptr;
+    if constexpr (MASK) {
+      if (row < N) {
+        const int b = bh / mk.H, h = bh - b * mk.H;
+        mrow = mk.bits + b * mk.sb + h * mk.sh + (long long)row * mk.sq + (kv_lo >> 5);
+      }
+    }
 
     if (row0 < N) {
       for (int j = 0; j < nkv; ++j) {
+        uint4 w = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if constexpr (MASK) {
+          if (mrow != nullptr) w = ld_mask16(mrow + 4 * j);
+        }
         ok = mbar_wait(&bar_s[t], (uint32_t)j & 1u, abort, status, kErrWaitS);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -423,6 +452,14 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
 
+        if constexpr (MASK) {
+          const bool whole = (w.x & w.y & w.z & w.w) == ~0u;
+          if (!__all_sync(0xffffffffu, whole)) {
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int c = 0; c < BN; ++c) s[c] = ((ww[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+          }
+        }
         const int key0 = kv_lo + j * BN;
         if ((key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0)) {
 #pragma unroll
@@ -551,10 +588,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int BN, bool BF16>
+template <int D, int BN, bool BF16, bool MASK = false>
 cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   using C = AttnCfg<D, BN>;
-  auto kern = attn_fwd_kernel<D, BN, BF16>;
+  auto kern = attn_fwd_kernel<D, BN, BF16, MASK>;
   static bool attr_set = false;
   if (!attr_set) {
     // The setmaxnreg split draws on the registers the CTA was launched with: refuse to
@@ -573,12 +610,16 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.BH,
                                                            a.N, a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
-                                                           a.out_f32, a.status);
+                                                           a.out_f32, a.mask, a.status);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t st) {
+  if (a.mask.bits != nullptr) {
+    if (block_n != 128) return cudaErrorInvalidValue;
+    return bf16 ? launch_attn_inst<D, 128, true, true>(a, st) : launch_attn_inst<D, 128, false, true>(a, st);
+  }
   switch (block_n) {
     case 32: return bf16 ? launch_attn_inst<D, 32, true>(a, st) : launch_attn_inst<D, 32, false>(a, st);
     case 64: return bf16 ? launch_attn_inst<D, 64, true>(a, st) : launch_attn_inst<D, 64, false>(a, st);

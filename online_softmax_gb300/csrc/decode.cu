@@ -24,8 +24,12 @@
 // overflow; the result is the same up to rounding.  p stays FP32 for the P.V products
 // here (there is no 16-bit operand to feed).
 //
+// The optional Boolean mask (one bit per key, packed) hides keys like the partition
+// bounds do: their score is -inf.  Lane i of every warp holds the mask word of tile
+// t0 + i for a window of 32 tiles; the tile's word is broadcast by a shuffle.
+//
 // Outputs: o_partial[p, bh, :] = o / l and lse_partial[p, bh] = m + log2(l), or +0 and
-// -inf when the partition holds no key.
+// -inf when the partition holds no visible key.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(kThreads)
     decode_splitk_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                          const uint16_t* __restrict__ v, void* __restrict__ o_partial,
                          float* __restrict__ lse_partial, long long BH, int Nkv, int P, int chunk,
-                         float scale_log2, int partial_f32, unsigned int* status) {
+                         float scale_log2, int partial_f32, const MaskArgs mk, unsigned int* status) {
   constexpr int EPL = D >= 32 ? D / 32 : 1;   // elements of a row per lane
   constexpr int LANES = D >= 32 ? 32 : D;     // lanes holding row elements
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -139,9 +143,17 @@ __global__ void __launch_bounds__(kThreads)
     float m = -INFINITY;  // running max in use (log2 units of the scaled score)
     float l = 0.f;        // this warp's partial denominator
     uint32_t seq = 0;     // monotone exchange counter of the warpgroup
+    const uint32_t* mrow = nullptr;  // mask word of the partition's first key tile
+    if (mk.bits != nullptr) {
+      const long long b = bh / mk.H, h = bh - b * mk.H;
+      mrow = mk.bits + b * mk.sb + h * mk.sh + (lo >> 5);
+    }
+    uint32_t mwin = ~0u;  // lane i: mask word of tile (t & ~31) + i
 
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % kStages;
+      if (mrow != nullptr && (t & 31) == 0) mwin = (t + lane < ntiles) ? __ldg(mrow + t + lane) : 0u;
+      const uint32_t mword = __shfl_sync(0xffffffffu, mwin, t & 31);
       // On a failed wait the warp keeps going through the loop without touching the
       // stage, so that all four warps still meet at every exchange barrier.
       const bool ok = mbar_wait(&sm.full[s], (uint32_t)(t / kStages) & 1u, abort, status, kErrWaitFull);
@@ -183,7 +195,7 @@ __global__ void __launch_bounds__(kThreads)
       g += __shfl_xor_sync(0xffffffffu, g, 2);
       g += __shfl_xor_sync(0xffffffffu, g, 1);
       const int my_key = (lane >> 2) & 7;  // key of this lane's score within the warp's 8
-      const bool valid = ok && key0 + my_key < nkeys;
+      const bool valid = ok && key0 + my_key < nkeys && ((mword >> (warp * kKeysPerWarp + my_key)) & 1u);
       const float sc = valid ? g * scale_log2 : -INFINITY;
       float tmax = sc;  // max over the 8 keys (lanes of one key agree)
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
@@ -258,7 +270,7 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(
       static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
       static_cast<const uint16_t*>(a.v), a.o_partial, a.lse_partial, a.BH, a.Nkv, a.P, a.chunk,
-      a.scale_log2, a.partial_dtype == kF32 ? 1 : 0, a.status);
+      a.scale_log2, a.partial_dtype == kF32 ? 1 : 0, a.mask, a.status);
   return cudaGetLastError();
 }
 

@@ -3,6 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 namespace oattn {
 
 enum DType : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
@@ -14,6 +16,19 @@ bool combine_supported(int depth, int in_dt);
 cudaError_t launch_combine(const void* o_partial, const float* lse_partial, void* o,
                            float* lse_out, int P, long long RH, int depth, int in_dt, int out_dt,
                            float lse_scale, bool pdl, cudaStream_t st);
+
+// ---- the optional Boolean mask, packed one bit per key (mask.cu packs it)
+// Row (b, h, q) of the mask starts at bits + b*sb + h*sh + q*sq (32-bit words; a stride
+// of 0 broadcasts); bit j of word w is key 32*w + j, set = visible.  A row holds
+// mask_words(Nkv) = 4*ceil(Nkv/128) words, so a 128-key tile is one aligned 16-byte load.
+struct MaskArgs {
+  const uint32_t* bits;  // nullptr: no mask
+  long long sb, sh, sq;
+  int H;                 // heads per batch entry (splits the flattened b*H + h index)
+};
+inline int mask_words(int nkv) { return 4 * ((nkv + 127) / 128); }
+cudaError_t launch_mask_pack(const uint8_t* mask, uint32_t* bits, long long rows, int nkv,
+                             long long row_stride, cudaStream_t st);
 
 // ---- one-query split-K decode on CUDA cores (decode.cu)
 struct DecodeArgs {
@@ -27,6 +42,7 @@ struct DecodeArgs {
   float scale_log2;    // scale * log2(e)
   int dtype;           // kF16 / kBF16
   int partial_dtype;   // kF32 / input dtype
+  MaskArgs mask;       // optional; row q = 0 of each (b, h)
   unsigned int* status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
@@ -42,6 +58,7 @@ struct AttnArgs {
   float scale_log2;
   int P, chunk;       // split mode when P > 0
   int out_f32;        // split mode: o_partial is float32
+  MaskArgs mask;      // optional (key tiles of 128 only)
   unsigned int* status;
 };
 // Instantiated per head dimension in attn_fwd_d{16,32,64,128}.cu.

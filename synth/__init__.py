@@ -23,6 +23,11 @@ Definition
   support bounded at about +-3.46.  ``mu + sigma * z`` is formed as one float32
   multiply then one float32 add (no fused multiply-add) on both sides.
 * Bernoulli(prob): the word's upper 32 bits compared with ``floor(prob * 2**32)``.
+* Boolean attention masks (True = the key is visible), four recipes: independent
+  Bernoulli entries; a sliding-window band |i - j| < w; block-sparse (one
+  Bernoulli draw per b x b block); key padding (per batch entry a visible
+  prefix of random length).  ``hide_rows`` hides every key of a Bernoulli subset
+  of rows, to exercise the fully masked case.
 * 16-bit storage: float32 rounded to bfloat16 or float16 with round-to-nearest-even.
 """
 from __future__ import annotations
@@ -38,6 +43,7 @@ NORM_SCALE = np.array([0x37DDB3D7], dtype=np.uint32).view(np.float32)[0]
 STREAM_Q, STREAM_K, STREAM_V = 1, 2, 3
 STREAM_LSE, STREAM_LSE_DROP, STREAM_ROW_DROP = 4, 5, 6
 STREAM_OPART = 7
+STREAM_MASK, STREAM_MASK_ROWS = 8, 9
 
 DTYPES = ("f16", "bf16", "f32")
 
@@ -174,4 +180,44 @@ def lse_partials_at(seed: int, P: int, RH: int, rh_idx, mu: float = 10.0, sigma:
         v = normal_at(seed, STREAM_LSE, j, mu, sigma)
         v[bernoulli_at(seed, STREAM_LSE_DROP, j, drop) | dead] = -np.inf
         out[p] = v
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Boolean masks (True = visible); host-side only, uploaded as bool tensors.
+# ---------------------------------------------------------------------------
+def mask_random(seed: int, shape, prob: float) -> np.ndarray:
+    """Independent Bernoulli(prob) entries; element index = flat index."""
+    n = int(np.prod(shape))
+    return bernoulli(seed, STREAM_MASK, 0, n, prob).reshape(shape)
+
+
+def mask_band(nq: int, nk: int, window: int) -> np.ndarray:
+    """Sliding window: query i sees keys j with |i - j| < window."""
+    i = np.arange(nq)[:, None]
+    j = np.arange(nk)[None, :]
+    return np.abs(i - j) < window
+
+
+def mask_blocks(seed: int, nq: int, nk: int, block: int, prob: float) -> np.ndarray:
+    """Block-sparse: each block x block tile is visible with probability prob."""
+    bq, bk = -(-nq // block), -(-nk // block)
+    tiles = bernoulli(seed, STREAM_MASK, 0, bq * bk, prob).reshape(bq, bk)
+    return np.repeat(np.repeat(tiles, block, axis=0), block, axis=1)[:nq, :nk]
+
+
+def key_padding(seed: int, batch: int, nk: int, min_len: int = 1) -> np.ndarray:
+    """[batch, 1, 1, nk]: batch entry b sees keys j < len_b, len_b uniform-ish in
+    [min_len, nk] (from the word's upper 32 bits)."""
+    w = words(seed, STREAM_MASK, 0, batch) >> np.uint64(32)
+    span = nk - min_len + 1
+    lens = min_len + (w % np.uint64(span)).astype(np.int64)
+    return (np.arange(nk)[None, :] < lens[:, None]).reshape(batch, 1, 1, nk)
+
+
+def hide_rows(seed: int, mask: np.ndarray, prob: float) -> np.ndarray:
+    """Copy of mask [..., nq, nk] with a Bernoulli(prob) subset of its rows fully hidden."""
+    out = np.array(mask, dtype=bool, copy=True)
+    rows = out.reshape(-1, out.shape[-1])
+    rows[bernoulli(seed, STREAM_MASK_ROWS, 0, rows.shape[0], prob)] = False
     return out

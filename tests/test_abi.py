@@ -123,3 +123,56 @@ def test_empty_problems_accept_null_pointers(lib):
 
 def test_device_error_needs_pointer(lib):
     assert lib.oattn_device_error(None) == 1
+
+
+# --- the optional Boolean mask -----------------------------------------------------
+@pytest.mark.parametrize("nkv,words", [(0, 0), (1, 4), (32, 4), (128, 4), (129, 8), (4096, 128), (4097, 132)])
+def test_mask_words(lib, nkv, words):
+    assert lib.attn_mask_words(nkv) == words
+
+
+def masked(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A2, lse=None, B=2, H=2, N=16, D=64, causal=0, scale=0.125, dt=1,
+             m=A, sb=0, sh=0, sq=4)
+    a.update(kw)
+    return lib.attn_fwd_masked(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                               a["causal"], a["scale"], a["dt"], a["m"], a["sb"], a["sh"], a["sq"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(m=None), 1), (dict(m=ctypes.c_void_p(0x1004)), 1), (dict(sq=2), 1), (dict(sb=-4), 1),
+    (dict(sh=6), 1), (dict(q=None), 1), (dict(D=96), 2), (dict(dt=2), 2), (dict(scale=-1.0), 1),
+])
+def test_attn_fwd_masked_rejects(lib, kw, expect):
+    assert masked(lib, **kw) == expect
+
+
+def splitk_masked(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=None, lse=None, B=1, H=1, Nq=1, Nkv=64, D=128, causal=0, scale=0.1, dt=1,
+             P=4, op=A2, lp=A2, pdt=2, m=A, sb=0, sh=0, sq=0)
+    a.update(kw)
+    return lib.attn_fwd_splitk_masked(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                                      a["Nkv"], a["D"], a["causal"], a["scale"], a["dt"], a["P"], a["op"],
+                                      a["lp"], a["pdt"], a["m"], a["sb"], a["sh"], a["sq"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(m=None), 1), (dict(m=MIS), 1), (dict(sh=1), 1), (dict(P=0), 1), (dict(op=None), 1),
+    (dict(causal=1, Nq=2, Nkv=3), 1),
+])
+def test_splitk_masked_rejects(lib, kw, expect):
+    assert splitk_masked(lib, **kw) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A, A2, -1, 10, 10), 1), ((A, A2, 4, -1, 10), 1), ((A, A2, 4, 10, 9), 1), ((None, A2, 4, 10, 10), 1),
+    ((A, None, 4, 10, 10), 1), ((A, ctypes.c_void_p(0x2008), 4, 10, 10), 1),
+    ((None, None, 0, 10, 10), 0), ((None, None, 4, 0, 0), 0),
+])
+def test_mask_pack_rejects(lib, args, expect):
+    assert lib.attn_mask_pack(*args, None) == expect
+
+
+def test_empty_masked_problems_accept_null_pointers(lib):
+    assert masked(lib, q=None, k=None, v=None, o=None, m=None, N=0) == 0
+    assert splitk_masked(lib, q=None, k=None, v=None, op=None, lp=None, m=None, Nq=0) == 0
