@@ -331,7 +331,40 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
     if args.part == "all":
         line["e2e"] = measure_e2e(torch, ops, q, k, v, args, world, dev)
         line["context"] = measure_sdpa(torch, q, k, v)
+        line["masked"] = measure_masked(torch, ops, synth, q, k, v, dev)
     return line
+
+
+def measure_masked(torch, ops, synth, q, k, v, dev):
+    """The optional Boolean mask on the same prefill inputs (causal): one shared N x N
+    mask per recipe, packed once; the kernel still computes every tile the causal rule
+    keeps, so the FLOP count is the unmasked one (dense-equivalent TFLOP/s)."""
+    import numpy as np
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    plain = lambda: ops.attn_fwd(q, k, v, o, lse, causal=CAUSAL)
+    for _ in range(3):
+        plain()
+    base, _ = time_launches(torch, plain, 20)
+    masks = {"all visible": np.ones((N, N), dtype=bool),
+             "sliding window 1024": synth.mask_band(N, N, 1024),
+             "random 50%": synth.mask_random(SEED, (N, N), 0.5),
+             "key padding [B,1,1,N], lengths >= N/2": synth.key_padding(SEED, B, N, N // 2)}
+    out = {"workload": WORKLOAD + ", shared Boolean mask", "unit": "TFLOP/s (dense-equivalent)",
+           "unmasked_tflops": FLOPS / base / 1e12, "results": []}
+    for name, m in masks.items():
+        mt = torch.from_numpy(np.array(m, dtype=bool, copy=True)).to(dev)
+        pack = lambda: ops.attn_mask_pack(mt)
+        pack_s, _ = time_launches(torch, pack, 5)
+        bits = pack()
+        fn = lambda: ops.attn_fwd_masked(q, k, v, o, bits, lse, causal=CAUSAL)
+        for _ in range(3):
+            fn()
+        med, _ = time_launches(torch, fn, 20)
+        out["results"].append({"mask": name, "tflops": FLOPS / med / 1e12, "vs_unmasked": base / med,
+                               "pack_us": pack_s * 1e6})
+    assert ops.device_error() == 0
+    return out
 
 
 def measure_sdpa(torch, q, k, v):
