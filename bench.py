@@ -493,14 +493,37 @@ def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps):
         # the same two kernels as two separate calls (plain stream order)
         fn_sep = lambda: (ops.attn_fwd_splitk(q, k, v, P, op, lp, None, None),
                           ops.splitk_combine(op, lp, o.view(RH, Dd), rows=Bd, heads=Hd))
+        # the merge inside the attention kernel (last CTA of each row-head)
+        counters = torch.zeros(ops.attn_splitk_counters(Bd, Hd, 1), dtype=torch.int32, device=dev)
+        fn_fused = lambda: ops.attn_fwd_splitk_fused(q, k, v, P, op, lp, counters, o, None)
         fn()
         fn_sep()
+        fn_fused()
         med, _ = time_launches(torch, fn, 10)
         med_sep, _ = time_launches(torch, fn_sep, 10)
+        med_fused, _ = time_launches(torch, fn_fused, 10)
         nbytes = 2 * Bd * Hd * Nkv * Dd * 2 + q.numel() * 2 + 2 * (P * RH * Dd * 4 + P * RH * 4) + o.numel() * 2
         gbs = nbytes / med / 1e9
         out["results"].append({"P": P, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"],
-                               "us_separate_calls": med_sep * 1e6, "pdl_speedup": med_sep / med})
+                               "us_separate_calls": med_sep * 1e6, "pdl_speedup": med_sep / med,
+                               "us_fused_merge": med_fused * 1e6, "fused_speedup": med / med_fused})
+    # one sequence: the merge is a larger share of a short step
+    small = []
+    for P in Ps:
+        q1, k1, v1 = q[:1], k[:1], v[:1]
+        op = torch.empty((P, Hd, Dd), dtype=torch.float32, device=dev)
+        lp = torch.empty((P, Hd), dtype=torch.float32, device=dev)
+        o1 = torch.empty_like(q1)
+        counters = torch.zeros(ops.attn_splitk_counters(1, Hd, 1), dtype=torch.int32, device=dev)
+        fn = lambda: ops.attn_fwd_splitk(q1, k1, v1, P, op, lp, o1, None)
+        fn_fused = lambda: ops.attn_fwd_splitk_fused(q1, k1, v1, P, op, lp, counters, o1, None)
+        fn()
+        fn_fused()
+        med, _ = time_launches(torch, fn, 20)
+        med_fused, _ = time_launches(torch, fn_fused, 20)
+        small.append({"P": P, "us": med * 1e6, "us_fused_merge": med_fused * 1e6, "fused_speedup": med / med_fused})
+    out["one_sequence"] = {"workload": "1 sequence x 1 query, 32 heads, 32768 keys, D=128, bf16",
+                           "results": small}
     assert ops.device_error() == 0
     fr = [r["frac"] for r in out["results"]]
     out["roofline"] = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "frac_min": min(fr),

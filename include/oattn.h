@@ -205,6 +205,38 @@ oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v,
                                     long long mask_stride_b, long long mask_stride_h,
                                     long long mask_stride_q, struct CUstream_st* stream);
 
+/*
+ * attn_fwd_splitk_fused - attn_fwd_splitk with the merge done inside the attention
+ * kernel instead of a second launch.  "fa4_splitk_combine" describes its kernel as the
+ * traditional, unfused (workspace) merge; here the CTA that finishes last among the P
+ * partitions of a group merges them ("Streaming attention and online state", Online
+ * statistics: independent summaries merge by rescaling to a common maximum).  Groups are
+ * row-heads for Nq == 1, and (head, 256 query rows) otherwise.
+ *
+ *   Arguments as attn_fwd_splitk, with o required, plus:
+ *   counters   device uint32 array of at least attn_splitk_counters(B, H, Nq) words
+ *              (B*H*Nq is always enough), 4-byte aligned, all ZERO before the first
+ *              call.  Each call counts the finished partitions of a group there and
+ *              the last one resets the word to zero, so a completed call leaves the
+ *              array zero for the next one.  After a call that reported an error
+ *              (oattn_device_error), clear the array again.  Calls that may overlap on
+ *              the GPU must use different counter arrays.
+ *   mask_bits  NULL, or the packed optional Boolean mask with its strides (as in
+ *              attn_fwd_splitk_masked).
+ * o_partial / lse_partial still receive every partition (the last CTA reads them back,
+ * normally from L2); they and the counters are owned by the caller.
+ */
+int attn_splitk_counters(int B, int H, int Nq);
+
+oattn_status attn_fwd_splitk_fused(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int Nq, int Nkv, int D,
+                                   int causal, float scale, oattn_dtype dtype, int P,
+                                   void* o_partial, float* lse_partial,
+                                   oattn_dtype partial_dtype, unsigned int* counters,
+                                   const unsigned int* mask_bits, long long mask_stride_b,
+                                   long long mask_stride_h, long long mask_stride_q,
+                                   struct CUstream_st* stream);
+
 /* Key chunk per partition used by attn_fwd_splitk (host-only, no GPU needed). */
 int splitk_chunk(int Nkv, int P);
 

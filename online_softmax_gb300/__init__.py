@@ -13,6 +13,7 @@ import os
 
 __all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine", "splitk_chunk",
            "attn_mask_words", "attn_mask_pack", "attn_fwd_masked", "attn_fwd_splitk_masked",
+           "attn_splitk_counters", "attn_fwd_splitk_fused",
            "device_error", "OattnError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -47,12 +48,15 @@ def _load():
     L.attn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, ll, ll, vp]
     L.attn_fwd_splitk_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i,
                                          vp, ll, ll, ll, vp]
+    L.attn_splitk_counters.argtypes = [i, i, i]
+    L.attn_fwd_splitk_fused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i, vp,
+                                        vp, ll, ll, ll, vp]
     L.oattn_status_string.argtypes = [i]
     L.oattn_status_string.restype = ctypes.c_char_p
     L.oattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine",
                  "splitk_chunk", "oattn_device_error", "attn_mask_words", "attn_mask_pack", "attn_fwd_masked",
-                 "attn_fwd_splitk_masked"):
+                 "attn_fwd_splitk_masked", "attn_splitk_counters", "attn_fwd_splitk_fused"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -290,6 +294,38 @@ def attn_fwd_splitk_masked(q, k, v, P, o_partial, lse_partial, mask, o=None, lse
                                     _stream(stream))
     _raise(st, "attn_fwd_splitk_masked")
     return o_partial, lse_partial, o, lse
+
+
+def attn_splitk_counters(B: int, H: int, Nq: int) -> int:
+    """Counter words attn_fwd_splitk_fused needs (at most B*H*Nq)."""
+    return lib.attn_splitk_counters(int(B), int(H), int(Nq))
+
+
+def attn_fwd_splitk_fused(q, k, v, P, o_partial, lse_partial, counters, o, lse=None, mask=None,
+                          causal=False, scale=None, stream=None):
+    """Split-K attention whose partitions are merged inside the attention kernel by the
+    last CTA of each group.  counters: int32 CUDA tensor with at least
+    attn_splitk_counters(B, H, Nq) elements, zero before the first call (each completed
+    call leaves it zero).  mask: None, or as in attn_fwd_splitk_masked.  Other arguments
+    as attn_fwd_splitk (o required)."""
+    import torch
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    _check(q, "q"); _check(k, "k", q.dtype, (B, H, Nkv, D)); _check(v, "v", q.dtype, (B, H, Nkv, D))
+    _check(o_partial, "o_partial", None, (P, B * H * Nq, D))
+    _check(lse_partial, "lse_partial", torch.float32, (P, B * H * Nq))
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, Nq))
+    _check(counters, "counters", torch.int32)
+    if counters.numel() < attn_splitk_counters(B, H, Nq):
+        raise ValueError(f"counters needs {attn_splitk_counters(B, H, Nq)} elements")
+    scale = D ** -0.5 if scale is None else float(scale)
+    keep, mp, sb, sh, sq = (None, None, 0, 0, 0) if mask is None else _mask_strides(mask, B, H, Nq, Nkv, stream)
+    st = lib.attn_fwd_splitk_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nkv, D,
+                                   int(bool(causal)), scale, _dtype_code(q.dtype), int(P), _ptr(o_partial),
+                                   _ptr(lse_partial), _dtype_code(o_partial.dtype), _ptr(counters), mp, sb, sh, sq,
+                                   _stream(stream))
+    _raise(st, "attn_fwd_splitk_fused")
+    return o, lse
 
 
 def device_error() -> int:

@@ -163,7 +163,7 @@ oattn_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o,
 oattn_status attn_fwd_splitk_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                                   int H, int Nq, int Nkv, int D, int causal, float scale, oattn_dtype dtype,
                                   int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
-                                  const MaskArgs& mk, cudaStream_t st) {
+                                  const MaskArgs& mk, unsigned int* counters, cudaStream_t st) {
   oattn_status s = attn_common_checks(q, k, v, B, H, Nq, Nkv, D, scale, dtype);
   if (s != OATTN_OK) return s;
   if (causal && Nq != Nkv) return OATTN_ERR_INVALID_ARG;
@@ -175,12 +175,19 @@ oattn_status attn_fwd_splitk_impl(const void* q, const void* k, const void* v, v
   if (!o_partial || !lse_partial) return OATTN_ERR_INVALID_ARG;
   if (!aligned(o_partial, 16) || !aligned(lse_partial, 4)) return OATTN_ERR_INVALID_ARG;
   if (o && (!aligned(o, 16) || (lse && !aligned(lse, 4)))) return OATTN_ERR_INVALID_ARG;
+  if (counters && (!o || !aligned(counters, 4))) return OATTN_ERR_INVALID_ARG;
   cudaError_t e;
   unsigned int* status = status_ptr(&e);
   if (!status) return OATTN_ERR_CUDA;
   const int BH = B * H;
   const int chunk = splitk_chunk(Nkv, P);
   const bool bf16 = dtype == OATTN_BF16;
+  FusedMerge fm{};
+  if (counters) {
+    fm.counters = counters;
+    fm.o = o;
+    fm.lse = lse;
+  }
   cudaError_t le;
   if (Nq == 1) {
     // One query row per head: matrix-vector work, streamed on CUDA cores.  (Causal with
@@ -194,6 +201,7 @@ oattn_status attn_fwd_splitk_impl(const void* q, const void* k, const void* v, v
     d.dtype = dtype;
     d.partial_dtype = partial_dtype;
     d.mask = mk;
+    d.fused = fm;
     d.status = status;
     le = launch_decode(d, st);
   } else {
@@ -215,10 +223,11 @@ oattn_status attn_fwd_splitk_impl(const void* q, const void* k, const void* v, v
     a.chunk = chunk;
     a.out_f32 = partial_dtype == OATTN_F32 ? 1 : 0;
     a.mask = mk;
+    a.fused = fm;
     le = launch_attn(a, 128, bf16, st);
   }
   if (le != cudaSuccess) return OATTN_ERR_CUDA;
-  if (o) {
+  if (o && !counters) {
     // The combine is a programmatic dependent of the producer just launched on this stream.
     le = launch_combine(o_partial, lse_partial, o, lse, P, (long long)BH * Nq, D, partial_dtype, dtype,
                         kLn2f, true, st);
@@ -298,7 +307,7 @@ oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* 
                              int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
                              struct CUstream_st* stream) {
   return attn_fwd_splitk_impl(q, k, v, o, lse, B, H, Nq, Nkv, D, causal, scale, dtype, P, o_partial,
-                              lse_partial, partial_dtype, MaskArgs{}, reinterpret_cast<cudaStream_t>(stream));
+                              lse_partial, partial_dtype, MaskArgs{}, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_mask_words(int Nkv) { return Nkv < 0 ? 0 : mask_words(Nkv); }
@@ -341,7 +350,29 @@ oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v,
   // With no keys every row is empty whatever the mask says: run unmasked.
   const MaskArgs mk = Nkv > 0 ? mask_args(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q, H) : MaskArgs{};
   return attn_fwd_splitk_impl(q, k, v, o, lse, B, H, Nq, Nkv, D, causal, scale, dtype, P, o_partial,
-                              lse_partial, partial_dtype, mk, reinterpret_cast<cudaStream_t>(stream));
+                              lse_partial, partial_dtype, mk, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_splitk_counters(int B, int H, int Nq) {
+  if (B < 1 || H < 1 || Nq < 1) return 0;
+  const long long n = (long long)B * H * (Nq == 1 ? 1 : (Nq + 255) / 256);
+  return n > 0x7fffffffLL ? -1 : (int)n;
+}
+
+oattn_status attn_fwd_splitk_fused(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                   int H, int Nq, int Nkv, int D, int causal, float scale, oattn_dtype dtype,
+                                   int P, void* o_partial, float* lse_partial, oattn_dtype partial_dtype,
+                                   unsigned int* counters, const unsigned int* mask_bits, long long mask_stride_b,
+                                   long long mask_stride_h, long long mask_stride_q, struct CUstream_st* stream) {
+  if (Nq > 0 && (!o || !counters)) return OATTN_ERR_INVALID_ARG;
+  MaskArgs mk{};
+  if (mask_bits && Nq > 0 && Nkv > 0) {
+    const oattn_status s = mask_checks(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q);
+    if (s != OATTN_OK) return s;
+    mk = mask_args(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q, H);
+  }
+  return attn_fwd_splitk_impl(q, k, v, o, lse, B, H, Nq, Nkv, D, causal, scale, dtype, P, o_partial,
+                              lse_partial, partial_dtype, mk, counters, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

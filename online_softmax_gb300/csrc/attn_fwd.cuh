@@ -256,6 +256,85 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// In-kernel split-K merge of one query row (rh = flat row-head index, RH row-heads per
+// partition): G = log2 sum_p 2^lse_p over the partitions, found in one pass with a
+// running maximum ("Streaming attention and online state", Online statistics, applied
+// to the partition summaries), then O = sum_p 2^(lse_p - G) O_p in 32-column chunks
+// ("fa4_splitk_combine").  Partitions with lse_p = -inf are skipped; a row with no
+// visible key anywhere gets +0 and -inf.  The partials were written by other CTAs in
+// this launch, so they are read through L2 (ld.global.cg), never a stale L1 line.
+template <int D, bool BF16>
+__device__ __forceinline__ void merge_row(const void* o_partial, const float* lse_partial, bool part_f32, int P,
+                                          size_t RH, size_t rh, void* o_final, float* lse_final) {
+  float m = -INFINITY, sum = 0.f;
+  for (int p = 0; p < P; ++p) {
+    const float l = __ldcg(lse_partial + (size_t)p * RH + rh);
+    if (l == -INFINITY) continue;
+    if (l > m) {
+      sum = fmaf(sum, ex2(m - l), 1.f);  // ex2(-inf) = 0 on the first live partition
+      m = l;
+    } else {
+      sum += ex2(l - m);
+    }
+  }
+  const float G = (m == -INFINITY) ? -INFINITY : m + lg2(sum);
+  constexpr int W = D < 32 ? D : 32;
+#pragma unroll 1
+  for (int c = 0; c < D / W; ++c) {
+    float acc[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) acc[i] = 0.f;
+    if (G != -INFINITY) {
+      // Two partitions per step, their loads issued together (independent L2 reads).
+#pragma unroll 1
+      for (int p0 = 0; p0 < P; p0 += 2) {
+        float x[2][W];
+        float w[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int p = p0 + u;
+          const float l = p < P ? __ldcg(lse_partial + (size_t)p * RH + rh) : -INFINITY;
+          w[u] = ex2(l - G);  // 0 for an empty partition (or none)
+          const size_t base = ((size_t)min(p, P - 1) * RH + rh) * D + (size_t)c * W;
+          if (part_f32) {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(o_partial) + base);
+#pragma unroll
+            for (int i = 0; i < W / 4; ++i) {
+              const float4 v4 = __ldcg(src + i);
+              x[u][4 * i] = v4.x;
+              x[u][4 * i + 1] = v4.y;
+              x[u][4 * i + 2] = v4.z;
+              x[u][4 * i + 3] = v4.w;
+            }
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o_partial) + base);
+#pragma unroll
+            for (int i = 0; i < W / 8; ++i) {
+              const uint4 v4 = __ldcg(src + i);
+              const uint32_t xw[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                x[u][8 * i + 2 * j] = unpack_lo<BF16>(xw[j]);
+                x[u][8 * i + 2 * j + 1] = unpack_hi<BF16>(xw[j]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          if (w[u] != 0.f) {  // skip empty partitions: their data never enters the sum
+#pragma unroll
+            for (int i = 0; i < W; ++i) acc[i] = fmaf(w[u], x[u][i], acc[i]);
+          }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < W; ++i) acc[i] += 0.f;
+    store_row_chunk<W, BF16>(static_cast<uint16_t*>(o_final) + rh * D + (size_t)c * W, acc, false);
+  }
+  if (lse_final != nullptr) lse_final[rh] = G * kLn2;
+}
+
 // 16 bytes of the packed mask (read-only path; rows of a shared mask stay in L2).
 __device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
   uint4 r;
@@ -265,12 +344,13 @@ __device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
   return r;
 }
 
-template <int D, int BN, bool BF16, bool MASK>
+template <int D, int BN, bool BF16, bool MASK, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     void* __restrict__ out, float* __restrict__ lse_out, int BH, int N, int Nkv, int causal,
-                    float scale_log2, int P, int chunk, int out_f32, const MaskArgs mk, unsigned int* status) {
+                    float scale_log2, int P, int chunk, int out_f32, const MaskArgs mk, const FusedMerge fm,
+                    unsigned int* status) {
   static_assert(!MASK || BN == 128, "the packed mask is read in 128-key tiles");
   using C = AttnCfg<D, BN>;
   constexpr int BM = C::BM;
@@ -281,6 +361,7 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ uint64_t bar_q, bar_s[2], bar_p[2], bar_o[2], bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_last;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -291,7 +372,7 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = tid & 31;
 
   // ---- which query tiles, head and key range this CTA owns
-  const bool split = P > 0;
+  constexpr bool split = SPLIT;  // split-K partitions (P > 0) or the plain forward
   const int nparts = split ? P : 1;
   const int npairs = (N + 2 * BM - 1) / (2 * BM);
   long long idx = blockIdx.x;
@@ -517,7 +598,7 @@ __global__ void __launch_bounds__(384, 1)
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       constexpr int W = D % 32 == 0 ? 32 : 16;
       if (ok && nkv > 0) tc_fence_after();
-      if (!split) {
+      if constexpr (!split) {
         // o / l -> 16-bit -> this tile's Q buffer (free now: the last S_t finished before
         // the last PV_t) in the output map's swizzled layout -> TMA store.  Every warp of
         // the warpgroup reaches the barrier, aborted or not; the store is skipped when
@@ -577,6 +658,29 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
+    if (split && fm.counters != nullptr) {  // (compiled into the split instances only)
+      // In-kernel merge: the CTA that finishes last among the P partitions of this
+      // (head, tile pair) merges its 256 rows.  Both softmax warpgroups take part (an
+      // empty second tile included) so that the barriers always complete.
+      // Publication: barrier, then one release fence and the counter update by thread 0;
+      // the last CTA's thread 0 fences again (acquire) before the barrier that releases
+      // the merge.
+      named_bar_sync(3, 256);
+      const long long g = (long long)bh * npairs + pair;
+      if (tid == 0) {
+        fence_acq_rel_gpu();
+        s_last = atomicAdd(fm.counters + g, 1u) == (unsigned)(P - 1);
+        if (s_last) {
+          fence_acq_rel_gpu();
+          fm.counters[g] = 0u;  // ready for the next call
+        }
+      }
+      named_bar_sync(3, 256);
+      if (s_last) {
+        if (row < N)
+          merge_row<D, BF16>(out, lse_out, out_f32 != 0, P, (size_t)BH * N, (size_t)bh * N + row, fm.o, fm.lse);
+      }
+    }
   }
 
   // ---- tear-down: everyone is done with TMEM before it is released
@@ -588,10 +692,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int BN, bool BF16, bool MASK = false>
+template <int D, int BN, bool BF16, bool MASK = false, bool SPLIT = false>
 cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   using C = AttnCfg<D, BN>;
-  auto kern = attn_fwd_kernel<D, BN, BF16, MASK>;
+  auto kern = attn_fwd_kernel<D, BN, BF16, MASK, SPLIT>;
   static bool attr_set = false;
   if (!attr_set) {
     // The setmaxnreg split draws on the registers the CTA was launched with: refuse to
@@ -610,13 +714,20 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.BH,
                                                            a.N, a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
-                                                           a.out_f32, a.mask, a.status);
+                                                           a.out_f32, a.mask, a.fused, a.status);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t st) {
-  if (a.mask.bits != nullptr) {
+  const bool mask = a.mask.bits != nullptr;
+  if (a.P > 0) {  // split-K partitions: key tiles of 128
+    if (block_n != 128) return cudaErrorInvalidValue;
+    if (mask)
+      return bf16 ? launch_attn_inst<D, 128, true, true, true>(a, st) : launch_attn_inst<D, 128, false, true, true>(a, st);
+    return bf16 ? launch_attn_inst<D, 128, true, false, true>(a, st) : launch_attn_inst<D, 128, false, false, true>(a, st);
+  }
+  if (mask) {
     if (block_n != 128) return cudaErrorInvalidValue;
     return bf16 ? launch_attn_inst<D, 128, true, true>(a, st) : launch_attn_inst<D, 128, false, true>(a, st);
   }

@@ -72,9 +72,11 @@ struct DecodeSmem {
   alignas(128) uint16_t v[kStages][kTK * D];
   float red[4][D];
   float xchg[2 * 2 * 128];
+  float lse_all[256];  // fused merge: the P partition LSEs of this row-head
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
+  int last;
 };
 
 template <int D, bool BF16>
@@ -82,7 +84,8 @@ __global__ void __launch_bounds__(kThreads)
     decode_splitk_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                          const uint16_t* __restrict__ v, void* __restrict__ o_partial,
                          float* __restrict__ lse_partial, long long BH, int Nkv, int P, int chunk,
-                         float scale_log2, int partial_f32, const MaskArgs mk, unsigned int* status) {
+                         float scale_log2, int partial_f32, const MaskArgs mk, const FusedMerge fm,
+                         unsigned int* status) {
   constexpr int EPL = D >= 32 ? D / 32 : 1;   // elements of a row per lane
   constexpr int LANES = D >= 32 ? 32 : D;     // lanes holding row elements
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -256,7 +259,72 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (tid == 0) lse_partial[(size_t)part * BH + bh] = (ltot > 0.f) ? m + lg2(ltot) : -INFINITY;
   }
+  if (fm.counters == nullptr) {
+    __syncthreads();
+    return;
+  }
+
+  // ---- in-kernel merge ("Streaming attention and online state", Online statistics:
+  // independent summaries merge by rescaling each with exp(m_i - m); here each partition
+  // is already normalised, so the weights are 2^(lse_p - G) as in "fa4_splitk_combine").
+  // The CTA's partial is published before its arrival is counted (barrier, then one
+  // release fence and the counter update by thread 0); the CTA that arrives last
+  // acquires the others' partials the same way and reads them back (from L2).
   __syncthreads();
+  if (tid == 0) {
+    fence_acq_rel_gpu();
+    sm.last = atomicAdd(fm.counters + bh, 1u) == (unsigned)(P - 1);
+    if (sm.last) {
+      fence_acq_rel_gpu();
+      fm.counters[bh] = 0u;  // ready for the next call
+    }
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  for (int p = tid; p < P; p += kThreads) sm.lse_all[p] = __ldcg(lse_partial + (size_t)p * BH + bh);
+  __syncthreads();
+  float mstar = -INFINITY;
+  for (int p = 0; p < P; ++p) mstar = fmaxf(mstar, sm.lse_all[p]);
+  float G = -INFINITY;
+  if (mstar != -INFINITY) {
+    float sum = 0.f;
+    for (int p = 0; p < P; ++p) sum += ex2(sm.lse_all[p] - mstar);  // 2^-inf = 0
+    G = mstar + lg2(sum);
+  }
+  if (tid < D) {
+    float acc = 0.f;
+    if (G != -INFINITY) {
+      // Eight partitions per step, their loads issued together (independent L2 reads).
+      constexpr int kU = 8;
+      for (int p0 = 0; p0 < P; p0 += kU) {
+        float x[kU];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          const int p = p0 + j;
+          x[j] = 0.f;
+          if (p < P) {
+            const size_t idx = ((size_t)p * BH + bh) * D + tid;
+            if (partial_f32) {
+              x[j] = __ldcg(static_cast<const float*>(o_partial) + idx);
+            } else {
+              const unsigned short b = __ldcg(static_cast<const unsigned short*>(o_partial) + idx);
+              x[j] = BF16 ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          const int p = p0 + j;
+          // an empty partition (lse -inf) contributes nothing
+          if (p < P && sm.lse_all[p] != -INFINITY) acc = fmaf(ex2(sm.lse_all[p] - G), x[j], acc);
+        }
+      }
+    }
+    const uint16_t y = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(acc + 0.f))
+                            : __half_as_ushort(__float2half_rn(acc + 0.f));
+    static_cast<uint16_t*>(fm.o)[(size_t)bh * D + tid] = y;
+  }
+  if (tid == 0 && fm.lse != nullptr) fm.lse[bh] = G * 0.6931471805599453f;
 }
 
 template <int D, bool BF16>
@@ -270,7 +338,7 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(
       static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
       static_cast<const uint16_t*>(a.v), a.o_partial, a.lse_partial, a.BH, a.Nkv, a.P, a.chunk,
-      a.scale_log2, a.partial_dtype == kF32 ? 1 : 0, a.mask, a.status);
+      a.scale_log2, a.partial_dtype == kF32 ? 1 : 0, a.mask, a.fused, a.status);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,15 @@ inline int mask_words(int nkv) { return 4 * ((nkv + 127) / 128); }
 cudaError_t launch_mask_pack(const uint8_t* mask, uint32_t* bits, long long rows, int nkv,
                              long long row_stride, cudaStream_t st);
 
+// ---- in-kernel split-K merge: the last CTA to finish a group of P partitions merges
+// them.  counters[g] counts the arrivals of group g (one per row-head in decode, one per
+// (head, pair of query tiles) in the tcgen05 split mode); the last arrival resets it to 0.
+struct FusedMerge {
+  unsigned int* counters;  // nullptr: no merge (partials only)
+  void* o;                 // [BH, Nq, D] in the input dtype
+  float* lse;              // [BH, Nq] natural log, or nullptr
+};
+
 // ---- one-query split-K decode on CUDA cores (decode.cu)
 struct DecodeArgs {
   const void* q;       // [BH, D]
@@ -43,6 +52,7 @@ struct DecodeArgs {
   int dtype;           // kF16 / kBF16
   int partial_dtype;   // kF32 / input dtype
   MaskArgs mask;       // optional; row q = 0 of each (b, h)
+  FusedMerge fused;    // optional in-kernel merge
   unsigned int* status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
@@ -59,6 +69,7 @@ struct AttnArgs {
   int P, chunk;       // split mode when P > 0
   int out_f32;        // split mode: o_partial is float32
   MaskArgs mask;      // optional (key tiles of 128 only)
+  FusedMerge fused;   // split mode: optional in-kernel merge
   unsigned int* status;
 };
 // Instantiated per head dimension in attn_fwd_d{16,32,64,128}.cu.

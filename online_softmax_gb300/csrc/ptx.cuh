@@ -217,6 +217,11 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 // 2^x with the MUFU approximation; results below 2^-126 flush to +0 (ftz), which costs
 // nothing here (such weights are far below FP32 resolution of any running sum) and
 // keeps the instruction a single MUFU operation.
+// GPU-scope acquire-release fence: with a CTA barrier before it, it publishes the
+// CTA's earlier global writes ahead of a following counter update (and, after reading
+// a counter, orders the reads that follow).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -176,3 +176,32 @@ def test_mask_pack_rejects(lib, args, expect):
 def test_empty_masked_problems_accept_null_pointers(lib):
     assert masked(lib, q=None, k=None, v=None, o=None, m=None, N=0) == 0
     assert splitk_masked(lib, q=None, k=None, v=None, op=None, lp=None, m=None, Nq=0) == 0
+
+
+# --- split-K with the in-kernel merge ------------------------------------------------
+@pytest.mark.parametrize("B,H,Nq,n", [(1, 1, 1, 1), (64, 32, 1, 2048), (1, 2, 256, 2), (1, 2, 257, 4),
+                                      (4, 32, 4096, 2048), (0, 1, 1, 0), (1, 1, 0, 0)])
+def test_splitk_counters(lib, B, H, Nq, n):
+    assert lib.attn_splitk_counters(B, H, Nq) == n
+    assert n <= max(B, 0) * H * Nq
+
+
+def fused(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A2, lse=None, B=1, H=1, Nq=1, Nkv=64, D=128, causal=0, scale=0.1, dt=1,
+             P=4, op=A2, lp=A2, pdt=2, c=A, m=None, sb=0, sh=0, sq=0)
+    a.update(kw)
+    return lib.attn_fwd_splitk_fused(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                                     a["Nkv"], a["D"], a["causal"], a["scale"], a["dt"], a["P"], a["op"],
+                                     a["lp"], a["pdt"], a["c"], a["m"], a["sb"], a["sh"], a["sq"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(o=None), 1), (dict(c=None), 1), (dict(c=ctypes.c_void_p(0x1002)), 1), (dict(P=0), 1),
+    (dict(m=MIS), 1), (dict(m=A, sq=3), 1), (dict(D=96), 2), (dict(op=None), 1),
+])
+def test_fused_rejects(lib, kw, expect):
+    assert fused(lib, **kw) == expect
+
+
+def test_fused_empty_accepts_null(lib):
+    assert fused(lib, q=None, k=None, v=None, o=None, op=None, lp=None, c=None, Nq=0) == 0
