@@ -16,9 +16,10 @@
 //   * A CTA owns two 128-row query tiles of one head (and one split-K partition in
 //     split mode).  Warps 0-3 and 4-7 are two softmax warpgroups, one per query tile;
 //     thread r of a warpgroup owns row r, which is TMEM lane r, so row max and row sum
-//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs; warps 10-11
-//     only complete the third warpgroup so that setmaxnreg can move its registers to
-//     the softmax warpgroups (216 per softmax thread).
+//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs, warp 10
+//     watches the K/V copies for the MMA issuer (see below); warps 10-11 also complete
+//     the third warpgroup so that setmaxnreg can move its registers to the softmax
+//     warpgroups (216 per softmax thread).
 //   * Q tiles are copied once; K and V tiles stream through a ring of shared-memory
 //     slots (K in even, V in odd slots) filled by cp.async.bulk.tensor with the
 //     128/64/32-byte swizzle that matches the tcgen05 shared-memory descriptors.
@@ -29,6 +30,12 @@
 //     ex2.approx each, sum the FP32 p, round p to the input dtype (cvt.rn, round to
 //     nearest even) and write it back over S (tcgen05.st) as the A operand of
 //     O_t += P V (M=128, N=D, K=BN, A from TMEM, B = V tile read MN-major).
+//   * The single MMA-issuing thread is the critical path: each mbarrier wait it makes
+//     costs it ~150-200 cycles while the tensor pipe streams shared memory, even when
+//     the phase has already completed.  So it waits once per group: bar_p[t] counts the
+//     128 softmax threads of tile t AND a watcher thread that has seen V_j and K_(j+1)
+//     land, so one completed phase means "P_t(j) written, PV_t(j) and S_t(j+1) may
+//     start".  The watcher never arrives for phase j before phase j - 1 completed.
 //   * The issue order S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... lets one
 //     warpgroup's softmax run while the tensor pipe works on the other tile.  A
 //     commit after S_t(j+1) also covers PV_t(j) (commits track every earlier MMA of the
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar_q, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
-      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_p[t], 129);  // 128 softmax threads + the K/V watcher
       mbar_init(&bar_o[t], 1);
     }
     mbar_init(&bar_done, 1);
@@ -458,7 +465,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t q_addr0 = smem_u32(smem), q_addr1 = q_addr0 + C::Q_BYTES;
       const uint32_t kv_addr = smem_u32(sKV);
       bool ok = mbar_wait(&bar_q, 0, abort, status, kErrWaitFull);
-      int k_ready = -1, v_ready = -1;
+      int k_ready = -1;
       if (ok && nkv0 > 0) {
         ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
         if (ok) issue_qk<C, BF16>(tmem, q_addr0, kv_addr, 0, 0, &bar_s[0]);
@@ -472,16 +479,11 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < 2; ++t) {
           const int nkv_t = t ? nkv1 : nkv0;
           if (j >= nkv_t) continue;
-          ok = wait_kv<NSLOT>(bar_full, 2 * j + 1, v_ready, abort, status) &&
-               mbar_wait(&bar_p[t], (uint32_t)j & 1u, abort, status, kErrWaitP);
+          ok = mbar_wait(&bar_p[t], (uint32_t)j & 1u, abort, status, kErrWaitP);
           if (!ok) break;
           issue_pv<C, BF16>(tmem, kv_addr, t, j);
           if (j == nkv_t - 1) tc_commit(&bar_o[t]);
-          if (j + 1 < nkv_t) {
-            ok = wait_kv<NSLOT>(bar_full, 2 * (j + 1), k_ready, abort, status);
-            if (!ok) break;
-            issue_qk<C, BF16>(tmem, t ? q_addr1 : q_addr0, kv_addr, t, j + 1, &bar_s[t]);
-          }
+          if (j + 1 < nkv_t) issue_qk<C, BF16>(tmem, t ? q_addr1 : q_addr0, kv_addr, t, j + 1, &bar_s[t]);
         }
         if (!ok) break;
         tc_commit(&bar_empty[(2 * j + 1) % NSLOT]);                      // V_j consumed
@@ -490,8 +492,30 @@ __global__ void __launch_bounds__(384, 1)
       // Drain every MMA this thread issued before TMEM is released.
       tc_commit(&bar_done);
       mbar_drain(&bar_done, 0, status);
+    } else if (warp == 10 && lane == 0 && nkv_max > 0) {
+      // ============================================================== K/V watcher
+      // Waits for the copies of V_j and K_(j+1) and adds one arrival to bar_p[t], so
+      // that the MMA issuer needs a single wait (P_t(j) written and its operands
+      // loaded) before PV_t(j) and S_t(j+1): every wait the issuing thread makes costs
+      // ~150-200 cycles while the tensor pipe reads shared memory, and the issuer is
+      // on the critical path.
+      bool ok = true;
+      for (int j = 0; ok && j < nkv_max; ++j)
+        for (int t = 0; ok && t < 2; ++t) {
+          const int nkv_t = t ? nkv1 : nkv0;
+          if (j >= nkv_t) continue;
+          // never arrive for phase j before phase j - 1 of bar_p[t] has completed
+          if (j > 0) ok = mbar_wait(&bar_p[t], (uint32_t)(j - 1) & 1u, abort, status, kErrWaitP);
+          const int nv = 2 * j + 1;
+          if (ok) ok = mbar_wait(&bar_full[nv % NSLOT], (uint32_t)(nv / NSLOT) & 1u, abort, status, kErrWaitFull);
+          if (ok && j + 1 < nkv_t) {
+            const int nk = 2 * (j + 1);
+            ok = mbar_wait(&bar_full[nk % NSLOT], (uint32_t)(nk / NSLOT) & 1u, abort, status, kErrWaitFull);
+          }
+          if (ok) mbar_arrive(&bar_p[t]);
+        }
     }
-    // warps 10-11 and the other lanes: nothing to do
+    // warp 11 and the other lanes: nothing to do (they donate registers)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX));
     // ================================================================ softmax warpgroups
