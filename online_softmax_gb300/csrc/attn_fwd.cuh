@@ -40,9 +40,11 @@
 //     warpgroup's softmax run while the tensor pipe works on the other tile.  A
 //     commit after S_t(j+1) also covers PV_t(j) (commits track every earlier MMA of the
 //     issuing thread), so when the softmax sees S_t(j+1) it may rescale O_t safely.
-//   * The rescale is lazy: a warp keeps its stale maximum until some row's maximum
-//     grows by more than kTauLazy (2^8), so p <= 256, and only then reloads O from
-//     TMEM, multiplies by alpha and stores it back.  Exact arithmetic is unchanged.
+//   * The stabiliser is lazy: m only has to keep p = 2^(x - m) bounded, so the common
+//     path computes no row maximum at all.  A warp takes the maximum only while some
+//     row has seen no key, or when a tile's row sum of p exceeds kPBound (2^15); then
+//     it redoes that tile against the exact new maximum and rescales O (TMEM load,
+//     multiply by alpha, store) and l.  Exact arithmetic is unchanged.
 //   * The epilogue writes o / l into the query tile's own (now free) shared memory in
 //     the swizzled layout of the output tensor map and stores it with one TMA copy per
 //     row chunk (rows past the end are clipped by the copy).  Split-K partials are
@@ -100,7 +102,9 @@ struct AttnCfg {
   static_assert(BN % 32 == 0 && D % 16 == 0, "tile shapes");
 };
 
-constexpr float kTauLazy = 8.0f;
+// Bound on a tile's row sum of p = 2^(x - m) before the stabiliser m must move (keeps
+// every p, and the 16-bit P operand, far from overflow; f16 stops at 65504).
+constexpr float kPBound = 32768.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kHeadGroup = 8;
 
@@ -574,42 +578,54 @@ __global__ void __launch_bounds__(384, 1)
             s[c] = vis ? s[c] : -INFINITY;
           }
         }
-        // row max: 8 independent chains of three-input max
-        float m8[8];
+        // The stabiliser m only has to keep every p = 2^(x - m) finite and within the
+        // 16-bit P operand's range; it need not be the row maximum.  So the maximum is
+        // taken only when some row of the warp has seen no key yet, or when this tile's
+        // exponentials exceed kPBound (p <= row sum): then the tile is redone against the
+        // exact new maximum, O and l are rescaled by alpha = 2^(m - m'), and P is stored
+        // again.  Exact arithmetic is unchanged; the common path has no max at all.
+        bool exact = !__all_sync(0xffffffffu, m != -INFINITY);
+        float rowsum;
+        for (;;) {
+          if (exact) {
+            // row max: 8 independent chains of three-input max
+            float m8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+            for (int i = 0; i < 8; ++i) m8[i] = s[i];
 #pragma unroll
-        for (int c = 8; c < BN; c += 16)
+            for (int c = 8; c < BN; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
-        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        const float mnew = fmaxf(m, mx * scale_log2);
-        const bool grow = (mnew - m) > kTauLazy;  // false for -inf - -inf (NaN)
-        const bool rescale = __any_sync(0xffffffffu, grow);
-        const float m_use = rescale ? mnew : m;
-        const float alpha = (m_use == m) ? 1.f : ex2(m - m_use);  // ex2(-inf) = 0
-        if (rescale && j > 0) tmem_scale_cols<D>(trow + col_o, alpha);
-        const float nbase = (m_use == -INFINITY) ? 0.f : -m_use;
-        // p = 2^(s*scale*log2e - m): the scale-and-shift runs on pairs (f32x2 FMA), the
-        // exponential on the MUFU, the row sum on pairs (f32x2 add) over four chains.
-        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c2 = 0; c2 < BN / 32; ++c2) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            ffma2(x0, x1, s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], p0, p1);
-            pk[i] = pack2<BF16>(p0, p1);
+              for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+            const float mnew = fmaxf(m, mx * scale_log2);
+            const float alpha = (mnew == m) ? 1.f : ex2(m - mnew);  // ex2(-inf) = 0
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) tmem_scale_cols<D>(trow + col_o, alpha);
+            l *= alpha;
+            m = mnew;
           }
-          tmem_st_x16(trow + col_s + c2 * 16, pk);
+          const float nbase = (m == -INFINITY) ? 0.f : -m;
+          // p = 2^(s*scale*log2e - m): the scale-and-shift runs on pairs (f32x2 FMA), the
+          // exponential on the MUFU, the row sum on pairs (f32x2 add) over four chains.
+          float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c2 = 0; c2 < BN / 32; ++c2) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              ffma2(x0, x1, s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], p0, p1);
+              pk[i] = pack2<BF16>(p0, p1);
+            }
+            tmem_st_x16(trow + col_s + c2 * 16, pk);
+          }
+          tmem_wait_st();
+          rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+          if (exact || __all_sync(0xffffffffu, rowsum <= kPBound)) break;  // NaN/inf fail the test
+          exact = true;
         }
-        tmem_wait_st();
-        const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        l = fmaf(alpha, l, rowsum);
-        m = m_use;
+        l += rowsum;
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
       }
