@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(384, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     void* __restrict__ out, float* __restrict__ lse_out, int BH, int N, int Nkv, int causal,
                     float scale_log2, int P, int chunk, int out_f32, const MaskArgs mk, const FusedMerge fm,
-                    unsigned int* status) {
+                    int ahead, unsigned int* status) {
   static_assert(!MASK || BN == 128, "the packed mask is read in 128-key tiles");
   using C = AttnCfg<D, BN>;
   constexpr int BM = C::BM;
@@ -386,15 +386,20 @@ __global__ void __launch_bounds__(384, 1)
   constexpr bool split = SPLIT;  // split-K partitions (P > 0) or the plain forward
   const int nparts = split ? P : 1;
   const int npairs = (N + 2 * BM - 1) / (2 * BM);
-  long long idx = blockIdx.x;
-  const int part = (int)(idx % nparts);
-  idx /= nparts;
-  const int group = (int)(idx / ((long long)kHeadGroup * npairs));
-  const int gheads = min(kHeadGroup, BH - group * kHeadGroup);
-  const int within = (int)(idx - (long long)group * kHeadGroup * npairs);
-  const int pair_rank = within / gheads;
-  const int bh = group * kHeadGroup + within % gheads;
-  const int pair = causal ? (npairs - 1 - pair_rank) : pair_rank;
+  // CTA index -> (head, query-tile pair, partition): groups of kHeadGroup heads, pairs
+  // longest first when causal.
+  auto cta_coords = [&](long long idx, int& bh_, int& pair_, int& part_) {
+    part_ = (int)(idx % nparts);
+    idx /= nparts;
+    const int group = (int)(idx / ((long long)kHeadGroup * npairs));
+    const int gheads = min(kHeadGroup, BH - group * kHeadGroup);
+    const int within = (int)(idx - (long long)group * kHeadGroup * npairs);
+    const int pair_rank = within / gheads;
+    bh_ = group * kHeadGroup + within % gheads;
+    pair_ = causal ? (npairs - 1 - pair_rank) : pair_rank;
+  };
+  int bh, pair, part;
+  cta_coords(blockIdx.x, bh, pair, part);
   const int kv_lo = split ? min(part * chunk, Nkv) : 0;
   const int kv_hi = split ? min(kv_lo + chunk, Nkv) : Nkv;
 
@@ -448,6 +453,15 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? row0_1 : row0_0,
                         bh);
+      // Warm L2 with the Q tiles of the CTA `ahead` launches later (one wave on), which
+      // is about when this SM or another picks it up: its first loads then hit L2.
+      if (ahead > 0 && (long long)blockIdx.x + ahead < (long long)gridDim.x) {
+        int bh2, pair2, part2;
+        cta_coords((long long)blockIdx.x + ahead, bh2, pair2, part2);
+        for (int t = 0; t < 2; ++t)
+          if (pair2 * 2 * BM + t * BM < N)
+            for (int c = 0; c < C::NCH; ++c) tma_prefetch_3d(&tm_q, c * C::CH, pair2 * 2 * BM + t * BM, bh2);
+      }
       int issued = 0;
       for (int n = 0; n < 2 * nkv_max; ++n) {
         const int slot = n % NSLOT;
@@ -732,6 +746,14 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// Streaming multiprocessors of the current device (0 if it cannot be queried).
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 template <int D, int BN, bool BF16, bool MASK = false, bool SPLIT = false>
 cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   using C = AttnCfg<D, BN>;
@@ -754,7 +776,7 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.BH,
                                                            a.N, a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
-                                                           a.out_f32, a.mask, a.fused, a.status);
+                                                           a.out_f32, a.mask, a.fused, sm_count(), a.status);
   return cudaGetLastError();
 }
 

@@ -138,3 +138,16 @@ def test_prefill_deterministic():
     o1, l1 = run_attn(q, k, v, True)
     o2, l2 = run_attn(q, k, v, True)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_growing_scores_move_the_stabiliser(causal, dtype):
+    """Scores that grow from key tile to key tile (K rows scaled up along the sequence)
+    make the kernel move its stabiliser again and again (redo a tile against the exact
+    maximum, rescale O and l); the result must still match the oracle."""
+    N, D = 1000, 64
+    qb, kb, vb = H.qkv_host(12, 1, 2, N, D, dtype)
+    ramp = 1.0 + np.arange(N, dtype=np.float64) / 40.0  # row maximum grows ~25x along the keys
+    kb = synth.round_to((synth.to_f64(kb, dtype) * ramp[None, None, :, None]).astype(np.float32), dtype)
+    check_full(qb, kb, vb, dtype, causal, what=f"growing scores {dtype} c{causal}")
