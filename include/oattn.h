@@ -70,6 +70,27 @@ oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       oattn_dtype dtype, struct CUstream_st* stream);
 
 /*
+ * attn_fwd_host - attn_fwd with the inputs and outputs in HOST memory: the heads are cut
+ * into chunks, and each chunk's copy in (host -> device), attention and copy out
+ * (device -> host) run on three internal streams so that one chunk's copies overlap its
+ * neighbours' attention.  Same result as attn_fwd, bit for bit.
+ *
+ *   q_h, k_h, v_h  [B, H, N, D] host inputs (pinned memory, or the copies do not overlap).
+ *   o_h            [B, H, N, D] host output;  lse_h  [B, H, N] float32 host output or NULL.
+ *   q_d, k_d, v_d, o_d, lse_d  device staging buffers of the same shapes, owned by the
+ *                  caller (lse_d NULL exactly when lse_h is NULL).
+ *   chunk_heads    heads (of the flattened B*H) per chunk; 0 picks ceil(B*H/8).
+ * The work starts after everything already queued on `stream`, and work queued on `stream`
+ * afterwards waits for the last copy out.  The first call on a device creates three
+ * streams and four events there (kept until the process exits); calls that overlap on one
+ * device share them and must be serialised by the caller.  Errors as attn_fwd.
+ */
+oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                           float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d,
+                           float* lse_d, int B, int H, int N, int D, int causal, float scale,
+                           oattn_dtype dtype, int chunk_heads, struct CUstream_st* stream);
+
+/*
  * attn_fwd_bn - attn_fwd with an explicit key-tile width block_n in {32, 64, 128}
  * ("A3. Tiled attention ...", section "Implement in four stages": BN is exposed as a
  * tuning choice).  block_n == 0 picks the default (128).  Results differ from attn_fwd

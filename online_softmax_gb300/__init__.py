@@ -13,7 +13,7 @@ import os
 
 __all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine", "splitk_chunk",
            "attn_mask_words", "attn_mask_pack", "attn_fwd_masked", "attn_fwd_splitk_masked",
-           "attn_splitk_counters", "attn_fwd_splitk_fused",
+           "attn_splitk_counters", "attn_fwd_splitk_fused", "attn_fwd_host",
            "device_error", "OattnError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -49,6 +49,7 @@ def _load():
     L.attn_fwd_splitk_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i,
                                          vp, ll, ll, ll, vp]
     L.attn_splitk_counters.argtypes = [i, i, i]
+    L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     L.attn_fwd_splitk_fused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i, vp,
                                         vp, ll, ll, ll, vp]
     L.oattn_status_string.argtypes = [i]
@@ -56,7 +57,7 @@ def _load():
     L.oattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine",
                  "splitk_chunk", "oattn_device_error", "attn_mask_words", "attn_mask_pack", "attn_fwd_masked",
-                 "attn_fwd_splitk_masked", "attn_splitk_counters", "attn_fwd_splitk_fused"):
+                 "attn_fwd_splitk_masked", "attn_splitk_counters", "attn_fwd_splitk_fused", "attn_fwd_host"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -125,6 +126,32 @@ def attn_fwd_bn(q, k, v, o, lse=None, causal=False, scale=None, block_n=0, strea
                          scale, _dtype_code(q.dtype), int(block_n), _stream(stream))
     _raise(st, "attn_fwd_bn")
     return o, lse
+
+
+def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d=None, causal=False, scale=None,
+                  chunk_heads=0, stream=None):
+    """Attention forward on HOST tensors (pinned CPU tensors [B, H, N, D]; lse_h [B, H, N]
+    float32 or None), through caller-owned device staging tensors of the same shapes: the
+    copies in and out overlap the attention of neighbouring chunks of heads."""
+    import torch
+    B, H, N, D = q_h.shape
+    for x, name in ((q_h, "q_h"), (k_h, "k_h"), (v_h, "v_h"), (o_h, "o_h")):
+        if x.is_cuda or not x.is_contiguous() or tuple(x.shape) != (B, H, N, D) or x.dtype != q_h.dtype:
+            raise ValueError(f"{name} must be a contiguous CPU tensor like q_h")
+    if (lse_h is None) != (lse_d is None):
+        raise ValueError("lse_h and lse_d go together")
+    if lse_h is not None and (lse_h.is_cuda or not lse_h.is_contiguous() or lse_h.dtype != torch.float32
+                              or tuple(lse_h.shape) != (B, H, N)):
+        raise ValueError("lse_h must be a contiguous float32 CPU tensor [B, H, N]")
+    _check(q_d, "q_d", q_h.dtype, q_h.shape); _check(k_d, "k_d", q_h.dtype, q_h.shape)
+    _check(v_d, "v_d", q_h.dtype, q_h.shape); _check(o_d, "o_d", q_h.dtype, q_h.shape)
+    _check(lse_d, "lse_d", torch.float32, (B, H, N))
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = lib.attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h), _ptr(q_d), _ptr(k_d),
+                           _ptr(v_d), _ptr(o_d), _ptr(lse_d), B, H, N, D, int(bool(causal)), scale,
+                           _dtype_code(q_h.dtype), int(chunk_heads), _stream(stream))
+    _raise(st, "attn_fwd_host")
+    return o_h, lse_h
 
 
 def attn_fwd(q, k, v, o, lse=None, causal=False, scale=None, stream=None):

@@ -41,6 +41,38 @@ unsigned int* status_ptr(cudaError_t* err) {
   return g_status_ptr[dev];
 }
 
+// Streams and events of the host-buffer entry point, created once per device (they are
+// scheduling resources, not memory; kept until the process exits).
+struct Pipe {
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, loaded = nullptr, done = nullptr, finished = nullptr;
+};
+Pipe g_pipe[kMaxDevices];
+
+Pipe* pipe_for_device(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  Pipe& p = g_pipe[dev];
+  if (p.finished == nullptr) {
+    const unsigned sf = cudaStreamNonBlocking, ef = cudaEventDisableTiming;
+    if ((*err = cudaStreamCreateWithFlags(&p.in, sf)) != cudaSuccess ||
+        (*err = cudaStreamCreateWithFlags(&p.comp, sf)) != cudaSuccess ||
+        (*err = cudaStreamCreateWithFlags(&p.out, sf)) != cudaSuccess ||
+        (*err = cudaEventCreateWithFlags(&p.start, ef)) != cudaSuccess ||
+        (*err = cudaEventCreateWithFlags(&p.loaded, ef)) != cudaSuccess ||
+        (*err = cudaEventCreateWithFlags(&p.done, ef)) != cudaSuccess ||
+        (*err = cudaEventCreateWithFlags(&p.finished, ef)) != cudaSuccess)
+      return nullptr;
+  }
+  return &p;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -283,6 +315,55 @@ oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, f
 oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                       int N, int D, int causal, float scale, oattn_dtype dtype, struct CUstream_st* stream) {
   return attn_fwd_bn(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, 0, stream);
+}
+
+oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                           void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d, int B, int H, int N, int D,
+                           int causal, float scale, oattn_dtype dtype, int chunk_heads,
+                           struct CUstream_st* stream) {
+  oattn_status s = attn_common_checks(q_d, k_d, v_d, B, H, N, N, D, scale, dtype);
+  if (s != OATTN_OK) return s;
+  if (chunk_heads < 0) return OATTN_ERR_INVALID_ARG;
+  if (N == 0) return OATTN_OK;
+  if (!q_h || !k_h || !v_h || !o_h || !o_d || !aligned(o_d, 16)) return OATTN_ERR_INVALID_ARG;
+  if ((lse_h == nullptr) != (lse_d == nullptr) || (lse_d && !aligned(lse_d, 4))) return OATTN_ERR_INVALID_ARG;
+  cudaError_t e;
+  Pipe* p = pipe_for_device(&e);
+  if (!p) return OATTN_ERR_CUDA;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const long long BH = (long long)B * H;
+  const long long ch = chunk_heads > 0 ? chunk_heads : (BH + 7) / 8;
+  const size_t head_bytes = (size_t)N * D * 2, lse_bytes = (size_t)N * 4;
+  auto off = [](const void* base, size_t bytes) { return static_cast<const char*>(base) + bytes; };
+  auto offm = [](void* base, size_t bytes) { return static_cast<char*>(base) + bytes; };
+  // Everything starts after the work already queued on the caller's stream.
+  if (cudaEventRecord(p->start, st) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess)
+    return OATTN_ERR_CUDA;
+  for (long long h0 = 0; h0 < BH; h0 += ch) {
+    const long long nh = (h0 + ch <= BH) ? ch : BH - h0;
+    const size_t o0 = (size_t)h0 * head_bytes, n0 = (size_t)nh * head_bytes;
+    // Copy in (one copy per tensor), attention on these heads, copy out: three streams,
+    // so the copies of one chunk overlap the attention of its neighbours.
+    if (cudaMemcpyAsync(offm(q_d, o0), off(q_h, o0), n0, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+        cudaMemcpyAsync(offm(k_d, o0), off(k_h, o0), n0, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+        cudaMemcpyAsync(offm(v_d, o0), off(v_h, o0), n0, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
+        cudaEventRecord(p->loaded, p->in) != cudaSuccess || cudaStreamWaitEvent(p->comp, p->loaded, 0) != cudaSuccess)
+      return OATTN_ERR_CUDA;
+    s = attn_fwd_impl(offm(q_d, o0), offm(k_d, o0), offm(v_d, o0), offm(o_d, o0),
+                      lse_d ? reinterpret_cast<float*>(offm(lse_d, (size_t)h0 * lse_bytes)) : nullptr, 1, (int)nh, N,
+                      D, causal, scale, dtype, 128, MaskArgs{}, p->comp);
+    if (s != OATTN_OK) return s;
+    if (cudaEventRecord(p->done, p->comp) != cudaSuccess || cudaStreamWaitEvent(p->out, p->done, 0) != cudaSuccess ||
+        cudaMemcpyAsync(offm(o_h, o0), off(o_d, o0), n0, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+      return OATTN_ERR_CUDA;
+    if (lse_d && cudaMemcpyAsync(offm(lse_h, (size_t)h0 * lse_bytes), off(lse_d, (size_t)h0 * lse_bytes),
+                                 (size_t)nh * lse_bytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+      return OATTN_ERR_CUDA;
+  }
+  // Work queued on the caller's stream afterwards starts once the last copy-out ends.
+  if (cudaEventRecord(p->finished, p->out) != cudaSuccess || cudaStreamWaitEvent(st, p->finished, 0) != cudaSuccess)
+    return OATTN_ERR_CUDA;
+  return OATTN_OK;
 }
 
 oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o, float* lse_out,

@@ -205,3 +205,23 @@ def test_fused_rejects(lib, kw, expect):
 
 def test_fused_empty_accepts_null(lib):
     assert fused(lib, q=None, k=None, v=None, o=None, op=None, lp=None, c=None, Nq=0) == 0
+
+
+def host(lib, **kw):
+    a = dict(qh=A, kh=A, vh=A, oh=A2, lh=None, qd=A, kd=A, vd=A, od=A2, ld=None, B=1, H=2, N=16, D=64, causal=0,
+             scale=0.125, dt=1, ch=0)
+    a.update(kw)
+    return lib.attn_fwd_host(a["qh"], a["kh"], a["vh"], a["oh"], a["lh"], a["qd"], a["kd"], a["vd"], a["od"], a["ld"],
+                             a["B"], a["H"], a["N"], a["D"], a["causal"], a["scale"], a["dt"], a["ch"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(qh=None), 1), (dict(oh=None), 1), (dict(od=None), 1), (dict(ch=-1), 1), (dict(lh=A), 1),
+    (dict(ld=A2), 1), (dict(D=96), 2), (dict(qd=MIS), 1), (dict(scale=0.0), 1),
+])
+def test_attn_fwd_host_rejects(lib, kw, expect):
+    assert host(lib, **kw) == expect
+
+
+def test_attn_fwd_host_empty(lib):
+    assert host(lib, qh=None, kh=None, vh=None, oh=None, qd=None, kd=None, vd=None, od=None, N=0) == 0
