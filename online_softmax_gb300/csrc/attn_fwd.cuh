@@ -618,19 +618,24 @@ __global__ void __launch_bounds__(384, 1)
             m = mnew;
           }
           const float nbase = (m == -INFINITY) ? 0.f : -m;
-          // p = 2^(s*scale*log2e - m): the scale-and-shift runs on pairs (f32x2 FMA), the
-          // exponential on the MUFU, the row sum on pairs (f32x2 add) over four chains.
+          // p = 2^(s*scale*log2e - m) per 32-column chunk: the scale-and-shift runs on
+          // pairs (f32x2 FMA), then all 32 exponentials on the MUFU (independent, so their
+          // latencies overlap), then the row sum on pairs (f32x2 add, four chains) and the
+          // 16-bit packing.
           float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c2 = 0; c2 < BN / 32; ++c2) {
             uint32_t pk[16];
+            float xx[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              ffma2(xx[2 * i], xx[2 * i + 1], s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xx[i] = ex2(xx[i]);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float x0, x1;
-              ffma2(x0, x1, s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], p0, p1);
-              pk[i] = pack2<BF16>(p0, p1);
+              fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], xx[2 * i], xx[2 * i + 1]);
+              pk[i] = pack2<BF16>(xx[2 * i], xx[2 * i + 1]);
             }
             tmem_st_x16(trow + col_s + c2 * 16, pk);
           }
