@@ -151,3 +151,24 @@ def test_growing_scores_move_the_stabiliser(causal, dtype):
     ramp = 1.0 + np.arange(N, dtype=np.float64) / 40.0  # row maximum grows ~25x along the keys
     kb = synth.round_to((synth.to_f64(kb, dtype) * ramp[None, None, :, None]).astype(np.float32), dtype)
     check_full(qb, kb, vb, dtype, causal, what=f"growing scores {dtype} c{causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_sampled(causal):
+    """N = 16384 (four times the prefill length), D = 128, bf16: sampled rows, tile
+    boundaries and the last row included, against the oracle."""
+    import synth.cuda as sc
+    B, Hh, N, D, seed = 1, 2, 16384, 128, 13
+    t = lambda: torch.empty((B, Hh, N, D), dtype=torch.bfloat16, device="cuda")
+    q = sc.fill_normal(t(), seed, synth.STREAM_Q, "bf16")
+    k = sc.fill_normal(t(), seed, synth.STREAM_K, "bf16")
+    v = sc.fill_normal(t(), seed, synth.STREAM_V, "bf16")
+    o, lse = run_attn(q, k, v, causal)
+    rows = np.unique(np.r_[0, 127, 128, 255, 256, 8191, 8192, 16383, np.random.default_rng(7).integers(0, N, 24)])
+    for bh in range(B * Hh):
+        qr = H.head_slice(seed, synth.STREAM_Q, bh, N, D, "bf16", rows)
+        kh = H.head_slice(seed, synth.STREAM_K, bh, N, D, "bf16")
+        vh = H.head_slice(seed, synth.STREAM_V, bh, N, D, "bf16")
+        O_ref, L_ref = oracle.attention_rows(qr, rows, kh, vh, 1.0 / math.sqrt(D), causal)
+        H.check16(H.to_f64(o[0, bh, rows]), O_ref, f"long bh{bh} O")
+        H.check32(H.to_f64(lse[0, bh, rows]), L_ref, f"long bh{bh} LSE")
