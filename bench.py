@@ -376,7 +376,7 @@ def measure_sdpa(torch, q, k, v):
         for _ in range(3):
             fn()
         med, _ = time_launches(torch, fn, 20)
-    except RuntimeError as e:  # a backend may be unavailable on this build
+    except RuntimeError as e:  # a backend may be missing from this PyTorch
         return {"sdpa": f"unavailable: {str(e).splitlines()[0][:120]}"}
     return {"sdpa_tflops": FLOPS / med / 1e12, "sdpa_ms": med * 1e3,
             "note": "torch SDPA, default backend selection, same inputs; context only"}

@@ -46,7 +46,7 @@ def test_single_head_n128_d64():
     check_full(qb, kb, vb, "bf16", False, what="n128")
 
 
-# Workshop checker matrix: D x N x dtype x causal x BN, three value regimes.
+# The workshop's case matrix: D x N x dtype x causal x BN, three value regimes.
 @pytest.mark.parametrize("regime", ["normal", "uniform", "large"])
 @pytest.mark.parametrize("block_n", [32, 64])
 @pytest.mark.parametrize("causal", [False, True])
