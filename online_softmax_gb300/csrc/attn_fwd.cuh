@@ -419,7 +419,10 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(&s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (tid == 0) {
+  // The copy thread sets up the barriers and starts the copies of Q and of the first ring
+  // of K/V tiles before the CTA-wide barrier, so they overlap the TMEM allocation.
+  const int first = min(NSLOT, 2 * nkv_max);  // K/V loads issued before the CTA barrier
+  if (warp == 8 && lane == 0) {
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
@@ -433,6 +436,19 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar_done, 1);
     s_abort = 0;
     fence_mbar_init();
+    if (nkv_max > 0) {
+      mbar_arrive_expect_tx(&bar_q, (nkv0 > 0 ? C::Q_BYTES : 0) + (nkv1 > 0 ? C::Q_BYTES : 0));
+      for (int t = 0; t < 2; ++t)
+        if ((t ? nkv1 : nkv0) > 0)
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? row0_1 : row0_0, bh);
+      for (int n = 0; n < first; ++n) {  // the ring starts empty: no wait
+        mbar_arrive_expect_tx(&bar_full[n], C::KV_BYTES);
+        const CUtensorMap* map = (n & 1) ? &tm_v : &tm_k;
+        uint8_t* dst = sKV + n * C::KV_BYTES;
+        for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * BN * C::SW, map, &bar_full[n], c * C::CH, kv_lo + (n >> 1) * BN, bh);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -447,12 +463,6 @@ __global__ void __launch_bounds__(384, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER));
     if (warp == 8 && lane == 0 && nkv_max > 0) {
       // ============================================================== TMA producer
-      mbar_arrive_expect_tx(&bar_q, (nkv0 > 0 ? C::Q_BYTES : 0) + (nkv1 > 0 ? C::Q_BYTES : 0));
-      for (int t = 0; t < 2; ++t)
-        if ((t ? nkv1 : nkv0) > 0)
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? row0_1 : row0_0,
-                        bh);
       // Warm L2 with the Q tiles of the CTA `ahead` launches later (one wave on), which
       // is about when this SM or another picks it up: its first loads then hit L2.
       if (ahead > 0 && (long long)blockIdx.x + ahead < (long long)gridDim.x) {
@@ -462,8 +472,8 @@ __global__ void __launch_bounds__(384, 1)
           if (pair2 * 2 * BM + t * BM < N)
             for (int c = 0; c < C::NCH; ++c) tma_prefetch_3d(&tm_q, c * C::CH, pair2 * 2 * BM + t * BM, bh2);
       }
-      int issued = 0;
-      for (int n = 0; n < 2 * nkv_max; ++n) {
+      int issued = first;
+      for (int n = first; n < 2 * nkv_max; ++n) {
         const int slot = n % NSLOT;
         const uint32_t use = n / NSLOT;
         if (!mbar_wait(&bar_empty[slot], (use & 1u) ^ 1u, abort, status, kErrWaitLoad)) break;
