@@ -262,7 +262,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_group_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until the bulk stores of this thread have read their shared-memory source (the
+// global writes complete on their own before the kernel does).
+__device__ __forceinline__ void bulk_wait_group_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -697,7 +699,7 @@ __global__ void __launch_bounds__(384, 1)
         if (r == 0 && *abort == 0) {
           for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, tile + c * BM * C::SW, c * C::CH, row0, bh);
           bulk_commit_group();
-          bulk_wait_group_0();
+          bulk_wait_group_read_0();
         }
         if (ok && row < N && lse_out != nullptr) {
           const float lse2 = (l > 0.f) ? m + lg2(l) : -INFINITY;
