@@ -358,13 +358,16 @@ cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P,
   const dim3 block(kCombineWarps * 32);
   auto* a = static_cast<const TIn*>(op);
   auto* c = static_cast<TOut*>(o);
-  // row-heads per warp: 8 at P = 2, 4 at P = 4 (the prefetch buffers grow with P)
-  const dim3 grid_small8((unsigned)((RH + kCombineWarps * 8 - 1) / (kCombineWarps * 8)));
-  const dim3 grid_small4((unsigned)((RH + kCombineWarps * 4 - 1) / (kCombineWarps * 4)));
+  // Row-heads per warp at P = 2 and 4 (measured): with 16-bit rows of one vector per lane
+  // fewer row-heads per warp, hence more warps, keep more of HBM busy at P = 2.
+  constexpr bool kWide = sizeof(TIn) == 2 && VPL == 1;
+  constexpr int R2 = kWide ? 4 : 8, R4 = 4;
+  const dim3 grid_small2((unsigned)((RH + kCombineWarps * R2 - 1) / (kCombineWarps * R2)));
+  const dim3 grid_small4((unsigned)((RH + kCombineWarps * R4 - 1) / (kCombineWarps * R4)));
   cudaError_t e;
   switch (P) {
-    case 2: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, 8>, grid_small8, block, st, a, lp, c, lo, RH, lse_scale); break;
-    case 4: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, 4>, grid_small4, block, st, a, lp, c, lo, RH, lse_scale); break;
+    case 2: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, R2>, grid_small2, block, st, a, lp, c, lo, RH, lse_scale); break;
+    case 4: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, R4>, grid_small4, block, st, a, lp, c, lo, RH, lse_scale); break;
     case 8: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 8>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
     case 16: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 16>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
     case 32: e = launch_maybe_pdl(pdl, splitk_combine_kernel<TIn, TOut, LPP, VPL, 32>, grid, block, st, a, lp, c, lo, P, RH, lse_scale); break;
