@@ -339,31 +339,39 @@ oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
   // Everything starts after the work already queued on the caller's stream.
   if (cudaEventRecord(p->start, st) != cudaSuccess || cudaStreamWaitEvent(p->in, p->start, 0) != cudaSuccess)
     return OATTN_ERR_CUDA;
-  for (long long h0 = 0; h0 < BH; h0 += ch) {
-    const long long nh = (h0 + ch <= BH) ? ch : BH - h0;
+  // Work queued on the caller's stream afterwards waits for everything enqueued here
+  // (on success the copy-out stream already follows the other two; after a failure part
+  // way through, all three are joined so that no copy outlives the call's buffers).
+  auto join = [&]() {
+    return cudaEventRecord(p->loaded, p->in) == cudaSuccess && cudaStreamWaitEvent(st, p->loaded, 0) == cudaSuccess &&
+           cudaEventRecord(p->done, p->comp) == cudaSuccess && cudaStreamWaitEvent(st, p->done, 0) == cudaSuccess &&
+           cudaEventRecord(p->finished, p->out) == cudaSuccess && cudaStreamWaitEvent(st, p->finished, 0) == cudaSuccess;
+  };
+  oattn_status result = OATTN_OK;
+  for (long long h0 = 0, nh = 0; h0 < BH && result == OATTN_OK; h0 += nh) {
+    nh = (h0 + ch <= BH) ? ch : BH - h0;
     const size_t o0 = (size_t)h0 * head_bytes, n0 = (size_t)nh * head_bytes;
     // Copy in (one copy per tensor), attention on these heads, copy out: three streams,
     // so the copies of one chunk overlap the attention of its neighbours.
     if (cudaMemcpyAsync(offm(q_d, o0), off(q_h, o0), n0, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
         cudaMemcpyAsync(offm(k_d, o0), off(k_h, o0), n0, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
         cudaMemcpyAsync(offm(v_d, o0), off(v_h, o0), n0, cudaMemcpyHostToDevice, p->in) != cudaSuccess ||
-        cudaEventRecord(p->loaded, p->in) != cudaSuccess || cudaStreamWaitEvent(p->comp, p->loaded, 0) != cudaSuccess)
-      return OATTN_ERR_CUDA;
-    s = attn_fwd_impl(offm(q_d, o0), offm(k_d, o0), offm(v_d, o0), offm(o_d, o0),
-                      lse_d ? reinterpret_cast<float*>(offm(lse_d, (size_t)h0 * lse_bytes)) : nullptr, 1, (int)nh, N,
-                      D, causal, scale, dtype, 128, MaskArgs{}, p->comp);
-    if (s != OATTN_OK) return s;
+        cudaEventRecord(p->loaded, p->in) != cudaSuccess || cudaStreamWaitEvent(p->comp, p->loaded, 0) != cudaSuccess) {
+      result = OATTN_ERR_CUDA;
+      break;
+    }
+    result = attn_fwd_impl(offm(q_d, o0), offm(k_d, o0), offm(v_d, o0), offm(o_d, o0),
+                           lse_d ? reinterpret_cast<float*>(offm(lse_d, (size_t)h0 * lse_bytes)) : nullptr, 1,
+                           (int)nh, N, D, causal, scale, dtype, 128, MaskArgs{}, p->comp);
+    if (result != OATTN_OK) break;
     if (cudaEventRecord(p->done, p->comp) != cudaSuccess || cudaStreamWaitEvent(p->out, p->done, 0) != cudaSuccess ||
-        cudaMemcpyAsync(offm(o_h, o0), off(o_d, o0), n0, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
-      return OATTN_ERR_CUDA;
-    if (lse_d && cudaMemcpyAsync(offm(lse_h, (size_t)h0 * lse_bytes), off(lse_d, (size_t)h0 * lse_bytes),
-                                 (size_t)nh * lse_bytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
-      return OATTN_ERR_CUDA;
+        cudaMemcpyAsync(offm(o_h, o0), off(o_d, o0), n0, cudaMemcpyDeviceToHost, p->out) != cudaSuccess ||
+        (lse_d && cudaMemcpyAsync(offm(lse_h, (size_t)h0 * lse_bytes), off(lse_d, (size_t)h0 * lse_bytes),
+                                  (size_t)nh * lse_bytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess))
+      result = OATTN_ERR_CUDA;
   }
-  // Work queued on the caller's stream afterwards starts once the last copy-out ends.
-  if (cudaEventRecord(p->finished, p->out) != cudaSuccess || cudaStreamWaitEvent(st, p->finished, 0) != cudaSuccess)
-    return OATTN_ERR_CUDA;
-  return OATTN_OK;
+  if (!join() && result == OATTN_OK) result = OATTN_ERR_CUDA;
+  return result;
 }
 
 oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o, float* lse_out,
