@@ -33,8 +33,9 @@
  *   - Every wait inside the kernels is bounded.  A wait that gives up records a code in
  *     a device status word and the kernel returns early (its outputs are then
  *     undefined); read and clear that word with oattn_device_error().
- *   - Not thread-safe across host threads for the first call on a new device (one-time
- *     set-up); afterwards calls are independent.
+ *   - Calls from several host threads are safe: the one-time set-up on each device
+ *     (the status word's address, kernel attributes, the host entry point's streams) is
+ *     guarded.  Calls that share a buffer or a workspace are not ordered by the library.
  */
 #ifndef OATTN_H
 #define OATTN_H
@@ -82,8 +83,11 @@ oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  *   chunk_heads    heads (of the flattened B*H) per chunk; 0 picks ceil(B*H/8).
  * The work starts after everything already queued on `stream`, and work queued on `stream`
  * afterwards waits for the last copy out.  The first call on a device creates three
- * streams and four events there (kept until the process exits); calls that overlap on one
- * device share them and must be serialised by the caller.  Errors as attn_fwd.
+ * streams and four events there (kept until the process exits).  Calls on one device
+ * share them: a call holds a per-device lock while it enqueues, so calls from several host
+ * threads are safe and their work runs one after the other on the internal streams (each
+ * still ordered after its own `stream`).  The staging buffers of calls that may overlap
+ * must not alias.  Errors as attn_fwd.
  */
 oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
                            float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d,

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -17,7 +18,7 @@ namespace {
 __device__ unsigned int g_status_word;
 
 constexpr int kMaxDevices = 64;
-unsigned int* g_status_ptr[kMaxDevices] = {};
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices] = {};
 std::mutex g_setup_mutex;
 
 // Device address of the status word for the current device (looked up once per device).
@@ -43,9 +44,12 @@ unsigned int* status_ptr(cudaError_t* err) {
 
 // Streams and events of the host-buffer entry point, created once per device (they are
 // scheduling resources, not memory; kept until the process exits).
+// A call holds `lock` while it enqueues, so that the record of an event and the waits on
+// it are not interleaved with another host thread's call on the same device.
 struct Pipe {
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, loaded = nullptr, done = nullptr, finished = nullptr;
+  std::mutex lock;
 };
 Pipe g_pipe[kMaxDevices];
 
@@ -330,6 +334,7 @@ oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
   cudaError_t e;
   Pipe* p = pipe_for_device(&e);
   if (!p) return OATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> enqueue(p->lock);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const long long BH = (long long)B * H;
   const long long ch = chunk_heads > 0 ? chunk_heads : (BH + 7) / 8;

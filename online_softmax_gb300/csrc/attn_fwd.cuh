@@ -64,6 +64,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -775,17 +776,23 @@ template <int D, int BN, bool BF16, bool MASK = false, bool SPLIT = false>
 cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   using C = AttnCfg<D, BN>;
   auto kern = attn_fwd_kernel<D, BN, BF16, MASK, SPLIT>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // The shared-memory attribute belongs to the function on one device: it is set once
+  // per device (one bit each; devices past 63 set it on every launch).
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0 || !(attr_set.load(std::memory_order_acquire) & bit)) {
     // The setmaxnreg split draws on the registers the CTA was launched with: refuse to
     // launch a build whose register count would make setmaxnreg.inc wait forever.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < C::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(bit, std::memory_order_release);
   }
   const long long npairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
   const long long blocks = npairs * a.BH * (a.P > 0 ? a.P : 1);

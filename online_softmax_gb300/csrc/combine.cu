@@ -351,6 +351,72 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   }
 }
 
+// Small P with short rows (NV < 32 vectors of 16 bytes per partition row): each lane owns
+// one vector of the row and folds all P partitions into it itself, so nothing crosses
+// lanes but the broadcast LSE loads; a warp covers 32/NV row-heads per pass and RPW
+// passes, with every load of all of them in flight before the first fold.
+template <typename TIn, typename TOut, int NV, int P_STATIC, int RPW>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    splitk_combine_lane_kernel(const TIn* __restrict__ o_partial, const float* __restrict__ lse_partial,
+                               TOut* __restrict__ out, float* __restrict__ lse_out, long long RH,
+                               float lse_scale) {
+  constexpr int E = Vec<TIn>::E;
+  constexpr int G = 32 / NV;  // row-heads per pass
+  constexpr int DEPTH = NV * E;
+  static_assert(NV < 32 && 32 % NV == 0, "a row-head takes a whole number of lanes");
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const long long rh0 = ((long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5)) * (RPW * G);
+  if (rh0 >= RH) return;  // whole warp leaves together
+  const int g = lane / NV, li = lane % NV;
+  const long long pstride = RH * (long long)DEPTH;
+
+  uint4 x[RPW][P_STATIC];
+  float lse[RPW][P_STATIC];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const long long rh = rh0 + r * G + g;
+    const bool valid = rh < RH;
+    const TIn* base = o_partial + rh * DEPTH + li * E;
+#pragma unroll
+    for (int p = 0; p < P_STATIC; ++p)
+      x[r][p] = valid ? __ldcs(reinterpret_cast<const uint4*>(base + p * pstride)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int p = 0; p < P_STATIC; ++p) lse[r][p] = valid ? __ldg(lse_partial + (long long)p * RH + rh) : -INFINITY;
+  }
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const long long rh = rh0 + r * G + g;
+    float m = lse[r][0];
+#pragma unroll
+    for (int p = 1; p < P_STATIC; ++p) m = fmaxf(m, lse[r][p]);
+    const bool dead = (m == -INFINITY);
+    const float msafe = dead ? 0.f : m;
+    float sum = 0.f;
+#pragma unroll
+    for (int p = 0; p < P_STATIC; ++p) sum += ex2(lse[r][p] - msafe);
+    const float Gl = dead ? -INFINITY : lg2(sum) + msafe;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int p = 0; p < P_STATIC; ++p) {
+      const float sc = dead ? 0.f : ex2(lse[r][p] - Gl);
+      float w[E];
+      widen_vec<TIn>(x[r][p], w);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(sc, (sc != 0.f) ? w[e] : 0.f, acc[e]);
+    }
+    if (rh < RH) {
+      float y[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) y[e] = dead ? 0.f : acc[e] + 0.f;
+      store_vec<TOut, E>(out + rh * DEPTH + li * E, y);
+      if (lse_out != nullptr && li == 0) lse_out[rh] = dead ? -INFINITY : Gl * lse_scale;
+    }
+  }
+}
+
 template <typename TIn, typename TOut, int LPP, int VPL>
 cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
                      float lse_scale, bool pdl, cudaStream_t st) {
@@ -365,6 +431,18 @@ cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P,
   const dim3 grid_small2((unsigned)((RH + kCombineWarps * R2 - 1) / (kCombineWarps * R2)));
   const dim3 grid_small4((unsigned)((RH + kCombineWarps * R4 - 1) / (kCombineWarps * R4)));
   cudaError_t e;
+  // Short rows at P = 2 and 4: one lane per vector, P partitions folded in the lane,
+  // 8 partition vectors in flight per lane (RPW = 8 / P passes).
+  constexpr int kLaneG = 32 / LPP;
+  const dim3 grid_lane2((unsigned)((RH + kCombineWarps * 4 * kLaneG - 1) / (kCombineWarps * 4 * kLaneG)));
+  const dim3 grid_lane4((unsigned)((RH + kCombineWarps * 2 * kLaneG - 1) / (kCombineWarps * 2 * kLaneG)));
+  if constexpr (LPP < 32 && VPL == 1) {
+    if (P == 2 || P == 4) {
+      e = (P == 2) ? launch_maybe_pdl(pdl, splitk_combine_lane_kernel<TIn, TOut, LPP, 2, 4>, grid_lane2, block, st, a, lp, c, lo, RH, lse_scale)
+                   : launch_maybe_pdl(pdl, splitk_combine_lane_kernel<TIn, TOut, LPP, 4, 2>, grid_lane4, block, st, a, lp, c, lo, RH, lse_scale);
+      return e != cudaSuccess ? e : cudaGetLastError();
+    }
+  }
   switch (P) {
     case 2: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, R2>, grid_small2, block, st, a, lp, c, lo, RH, lse_scale); break;
     case 4: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 4, R4>, grid_small4, block, st, a, lp, c, lo, RH, lse_scale); break;

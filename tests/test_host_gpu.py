@@ -63,3 +63,44 @@ def test_host_against_oracle_without_lse():
     O, _ = oracle.attention(synth.to_f64(qb, "f16"), synth.to_f64(kb, "f16"), synth.to_f64(vb, "f16"),
                             1.0 / math.sqrt(D), True)
     H.check16(H.to_f64(oh), O, "host path O")
+
+
+def test_host_calls_from_four_threads():
+    """Four host threads call attn_fwd_host at once, each with its own stream and staging
+    buffers; the calls share the library's internal streams and events, and each result
+    still equals attn_fwd on device buffers bit for bit."""
+    import threading
+    B, Hh, N, D = 1, 6, 300, 64
+    cases = []
+    for i in range(4):
+        qb, kb, vb = H.qkv_host(170 + i, B, Hh, N, D, "bf16")
+        qh, kh, vh, oh, lh = host_tensors(qb, kb, vb, "bf16", True)
+        staging = [torch.empty(qh.shape, dtype=qh.dtype, device="cuda") for _ in range(4)]
+        staging.append(torch.empty(qh.shape[:3], dtype=torch.float32, device="cuda"))
+        cases.append(((qb, kb, vb), (qh, kh, vh, oh, lh), staging, torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(case):
+        _, (qh, kh, vh, oh, lh), (qd, kd, vd, od, ld), st = case
+        try:
+            for _ in range(5):
+                ops.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, causal=True, chunk_heads=2, stream=st)
+            st.synchronize()
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(c,)) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for (qb, kb, vb), (_, _, _, oh, lh), _, _ in cases:
+        q, k, v = (H.to_device(x, "bf16") for x in (qb, kb, vb))
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+        ops.attn_fwd(q, k, v, o, lse, causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())

@@ -88,7 +88,7 @@ def test_combine_full_size(P, dtype):
     assert torch.all(torch.isneginf(g[torch.from_numpy(dead).cuda()]))
 
 
-@pytest.mark.parametrize("P", [1, 3, 5, 64, 100, 256])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 64, 100, 256])
 @pytest.mark.parametrize("depth,in_dt,out_dt", [(128, "f32", "f32"), (64, "bf16", "bf16"),
                                                 (256, "f16", "f32"), (32, "f32", "bf16"),
                                                 (16, "bf16", "f16"), (128, "bf16", "f32")])
