@@ -40,6 +40,14 @@
 #ifndef OATTN_H
 #define OATTN_H
 
+/* The library is built with hidden symbol visibility; these entry points alone are
+ * exported. */
+#if defined(__GNUC__)
+#define OATTN_API __attribute__((visibility("default")))
+#else
+#define OATTN_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -66,7 +74,7 @@ typedef enum { OATTN_F16 = 0, OATTN_BF16 = 1, OATTN_F32 = 2 } oattn_dtype;
  * Returns OATTN_OK, OATTN_ERR_INVALID_ARG or OATTN_ERR_UNSUPPORTED (dtype f32, other D),
  * or OATTN_ERR_CUDA.
  */
-oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+OATTN_API oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                       int B, int H, int N, int D, int causal, float scale,
                       oattn_dtype dtype, struct CUstream_st* stream);
 
@@ -89,7 +97,7 @@ oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  * still ordered after its own `stream`).  The staging buffers of calls that may overlap
  * must not alias.  Errors as attn_fwd.
  */
-oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+OATTN_API oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
                            float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d,
                            float* lse_d, int B, int H, int N, int D, int causal, float scale,
                            oattn_dtype dtype, int chunk_heads, struct CUstream_st* stream);
@@ -100,7 +108,7 @@ oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  * tuning choice).  block_n == 0 picks the default (128).  Results differ from attn_fwd
  * only by floating-point summation order.
  */
-oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse,
+OATTN_API oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int H, int N, int D, int causal, float scale,
                          oattn_dtype dtype, int block_n, struct CUstream_st* stream);
 
@@ -123,7 +131,7 @@ oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, f
  * o_partial and lse_partial are scratch owned by the caller and must not overlap q, k, v,
  * o or lse.
  */
-oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* o, float* lse,
+OATTN_API oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int H, int Nq, int Nkv, int D, int causal, float scale,
                              oattn_dtype dtype, int P, void* o_partial, float* lse_partial,
                              oattn_dtype partial_dtype, struct CUstream_st* stream);
@@ -143,7 +151,7 @@ oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* 
  *   1 <= P <= 256; rows, heads >= 1; depth a power of two with depth*sizeof(in_dtype)
  *   between 32 and 1024 bytes (f32: 8..256, f16/bf16: 16..512).
  */
-oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o,
+OATTN_API oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o,
                             float* lse_out, int P, int rows, int heads, int depth,
                             oattn_dtype in_dtype, oattn_dtype out_dtype,
                             struct CUstream_st* stream);
@@ -167,7 +175,7 @@ oattn_status splitk_combine(const void* o_partial, const float* lse_partial, voi
  *   streams, or different host threads on one device) race and must be serialised by
  *   the caller.  Each call rewrites every partial it reads, so no clearing is needed.
  */
-oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+OATTN_API oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                                      int B, int H, int Nq, int Nkv, int D, int causal, float scale,
                                      oattn_dtype dtype, int P, struct CUstream_st* stream);
 
@@ -190,7 +198,7 @@ oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, const void* v
  *   mask_stride_q = 0).  mask_bits is a device pointer on a 16-byte boundary, owned by
  *   the caller and only read.
  */
-int attn_mask_words(int Nkv);
+OATTN_API int attn_mask_words(int Nkv);
 
 /*
  * attn_mask_pack - pack a byte mask into the bit layout above.
@@ -202,7 +210,7 @@ int attn_mask_words(int Nkv);
  * rows == 0 or Nkv == 0 is a no-op.  Returns OATTN_ERR_INVALID_ARG for negative sizes,
  * null or misaligned pointers or row_stride < Nkv.
  */
-oattn_status attn_mask_pack(const void* mask, unsigned int* bits, long long rows, int Nkv,
+OATTN_API oattn_status attn_mask_pack(const void* mask, unsigned int* bits, long long rows, int Nkv,
                             long long row_stride, struct CUstream_st* stream);
 
 /*
@@ -210,7 +218,7 @@ oattn_status attn_mask_pack(const void* mask, unsigned int* bits, long long rows
  *   Arguments as attn_fwd, plus the packed mask and its strides (above); the mask is
  *   required (non-NULL) when N > 0.  Causal and mask may be combined.
  */
-oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+OATTN_API oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int H, int N, int D, int causal, float scale,
                              oattn_dtype dtype, const unsigned int* mask_bits,
                              long long mask_stride_b, long long mask_stride_h,
@@ -222,7 +230,7 @@ oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* 
  *   stores O_p = +0 and lse_p = -inf, like an empty partition.  Nq == 1 reads only
  *   row q = 0 of each (b, h), so mask_stride_q is not used there.
  */
-oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v, void* o,
+OATTN_API oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v, void* o,
                                     float* lse, int B, int H, int Nq, int Nkv, int D,
                                     int causal, float scale, oattn_dtype dtype, int P,
                                     void* o_partial, float* lse_partial,
@@ -251,9 +259,9 @@ oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v,
  * o_partial / lse_partial still receive every partition (the last CTA reads them back,
  * normally from L2); they and the counters are owned by the caller.
  */
-int attn_splitk_counters(int B, int H, int Nq);
+OATTN_API int attn_splitk_counters(int B, int H, int Nq);
 
-oattn_status attn_fwd_splitk_fused(const void* q, const void* k, const void* v, void* o,
+OATTN_API oattn_status attn_fwd_splitk_fused(const void* q, const void* k, const void* v, void* o,
                                    float* lse, int B, int H, int Nq, int Nkv, int D,
                                    int causal, float scale, oattn_dtype dtype, int P,
                                    void* o_partial, float* lse_partial,
@@ -263,10 +271,10 @@ oattn_status attn_fwd_splitk_fused(const void* q, const void* k, const void* v, 
                                    struct CUstream_st* stream);
 
 /* Key chunk per partition used by attn_fwd_splitk (host-only, no GPU needed). */
-int splitk_chunk(int Nkv, int P);
+OATTN_API int splitk_chunk(int Nkv, int P);
 
 /* Human-readable name of a status code (static string). */
-const char* oattn_status_string(oattn_status s);
+OATTN_API const char* oattn_status_string(oattn_status s);
 
 /*
  * oattn_device_error - read and clear the device status word of the current device.
@@ -274,7 +282,7 @@ const char* oattn_status_string(oattn_status s);
  * since the last call, else a nonzero site code; returns OATTN_ERR_TIMEOUT in that case,
  * OATTN_OK otherwise, or OATTN_ERR_CUDA if the device could not be queried.
  */
-oattn_status oattn_device_error(int* code);
+OATTN_API oattn_status oattn_device_error(int* code);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,8 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:oattn_status|int|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:OATTN_API\s+)?(?:oattn_status|int|const char\*)\s+(\w+)\s*\(", text,
+                                 flags=re.M)))
 
 
 def test_header_declares_the_entry_points():
@@ -39,6 +40,23 @@ def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(__import__("online_softmax_gb300").library_path)
     for n in declared_functions():
         assert hasattr(raw, n), f"{n} declared in oattn.h but not exported"
+
+
+def test_library_exports_nothing_else(lib):
+    """Only the declared entry points are visible: internal symbols (launchers, per-kernel
+    set-up state) stay private, so two builds loaded in one process do not share them."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", __import__("online_softmax_gb300").library_path],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    exported = {n for n in exported if not n.startswith("_")}
+    assert exported == set(declared_functions())
+    assert not any(line.split()[1] == "u" for line in out.splitlines() if len(line.split()) >= 3), \
+        "a unique (process-wide) symbol is exported"
 
 
 @pytest.mark.parametrize("nkv", [0, 1, 127, 128, 1000, 4096, 32768, 100000])

@@ -172,3 +172,25 @@ def test_long_sequence_sampled(causal):
         O_ref, L_ref = oracle.attention_rows(qr, rows, kh, vh, 1.0 / math.sqrt(D), causal)
         H.check16(H.to_f64(o[0, bh, rows]), O_ref, f"long bh{bh} O")
         H.check32(H.to_f64(lse[0, bh, rows]), L_ref, f"long bh{bh} LSE")
+
+
+def test_second_copy_of_the_library_in_one_process(tmp_path):
+    """A second copy of the library loaded next to the first keeps its own per-device
+    set-up (kernel attributes, status word): both copies launch and agree bit for bit."""
+    import ctypes
+    import shutil
+    copy = tmp_path / "liboattn_copy.so"
+    shutil.copy(ops.library_path, copy)
+    L2 = ctypes.CDLL(str(copy))
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L2.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    qb, kb, vb = H.qkv_host(190, 1, 2, 300, 128, "bf16")
+    q, k, v = (H.to_device(x, "bf16") for x in (qb, kb, vb))
+    o1, l1 = run_attn(q, k, v, True)
+    o2, l2 = torch.empty_like(q), torch.empty_like(l1)
+    st = torch.cuda.current_stream().cuda_stream
+    rc = L2.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(), 1, 2, 300, 128, 1,
+                     1.0 / math.sqrt(128), ops.BF16, st)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
