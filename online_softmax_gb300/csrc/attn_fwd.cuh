@@ -631,26 +631,29 @@ __global__ void __launch_bounds__(384, 1)
             m = mnew;
           }
           const float nbase = (m == -INFINITY) ? 0.f : -m;
-          // p = 2^(s*scale*log2e - m) per 32-column chunk: the scale-and-shift runs on
-          // pairs (f32x2 FMA), then all 32 exponentials on the MUFU (independent, so their
+          // p = 2^(s*scale*log2e - m) per chunk of CW columns: the scale-and-shift runs on
+          // pairs (f32x2 FMA), then all CW exponentials on the MUFU (independent, so their
           // latencies overlap), then the row sum on pairs (f32x2 add, four chains) and the
-          // 16-bit packing.
+          // 16-bit packing.  Chunks of 64 columns measured ~1% faster than chunks of 32 or
+          // 16 (more independent work between the dependent stages).
+          constexpr int CW = BN < 64 ? BN : 64;
           float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c2 = 0; c2 < BN / 32; ++c2) {
-            uint32_t pk[16];
-            float xx[32];
+          for (int c2 = 0; c2 < BN / CW; ++c2) {
+            uint32_t pk[CW / 2];
+            float xx[CW];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              ffma2(xx[2 * i], xx[2 * i + 1], s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
+            for (int i = 0; i < CW / 2; ++i)
+              ffma2(xx[2 * i], xx[2 * i + 1], s[c2 * CW + 2 * i], s[c2 * CW + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) xx[i] = ex2(xx[i]);
+            for (int i = 0; i < CW; ++i) xx[i] = ex2(xx[i]);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < CW / 2; ++i) {
               fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], xx[2 * i], xx[2 * i + 1]);
               pk[i] = pack2<BF16>(xx[2 * i], xx[2 * i + 1]);
             }
-            tmem_st_x16(trow + col_s + c2 * 16, pk);
+            if constexpr (CW == 64) tmem_st_x32(trow + col_s + c2 * 32, pk);
+            else tmem_st_x16(trow + col_s + c2 * 16, pk);
           }
           tmem_wait_st();
           rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
