@@ -284,6 +284,22 @@ OATTN_API const char* oattn_status_string(oattn_status s);
  */
 OATTN_API oattn_status oattn_device_error(int* code);
 
+/*
+ * oattn_selftest_wait - exercises the bounded-wait failure path on the device without a
+ * fault: one thread waits for an mbarrier phase that can never complete (two arrivals
+ * expected, one made); after the library's wait limit (2 s) the wait gives up, records
+ * the site code OATTN_SELFTEST_SITE in the device status word and raises its CTA's abort
+ * flag; a second warp, waiting on a barrier nothing arrives on, leaves through that flag.
+ * The kernel then returns and the context stays usable: oattn_device_error() reports
+ * OATTN_ERR_TIMEOUT with code OATTN_SELFTEST_SITE.
+ *   flags  optional device array of 2 ints (NULL allowed): 1 where a wait completed,
+ *          0 where it gave up (both 0 after a correct run).
+ * Returns OATTN_OK once the kernel is enqueued, OATTN_ERR_INVALID_ARG for a misaligned
+ * flags pointer, OATTN_ERR_CUDA for a failed launch.
+ */
+#define OATTN_SELFTEST_SITE 0x1F0
+OATTN_API oattn_status oattn_selftest_wait(int* flags, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

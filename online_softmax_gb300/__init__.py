@@ -55,9 +55,11 @@ def _load():
     L.oattn_status_string.argtypes = [i]
     L.oattn_status_string.restype = ctypes.c_char_p
     L.oattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    L.oattn_selftest_wait.argtypes = [vp, vp]
     for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine",
                  "splitk_chunk", "oattn_device_error", "attn_mask_words", "attn_mask_pack", "attn_fwd_masked",
-                 "attn_fwd_splitk_masked", "attn_splitk_counters", "attn_fwd_splitk_fused", "attn_fwd_host"):
+                 "attn_fwd_splitk_masked", "attn_splitk_counters", "attn_fwd_splitk_fused", "attn_fwd_host",
+                 "oattn_selftest_wait"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -353,6 +355,21 @@ def attn_fwd_splitk_fused(q, k, v, P, o_partial, lse_partial, counters, o, lse=N
                                    _stream(stream))
     _raise(st, "attn_fwd_splitk_fused")
     return o, lse
+
+
+SELFTEST_SITE = 0x1F0  # site code recorded by selftest_wait's wait
+
+
+def selftest_wait(flags=None, stream=None):
+    """Run the device self-test of the bounded-wait failure path (about 2 s): a wait on a
+    phase that never completes gives up, records SELFTEST_SITE in the device status word
+    and the kernel returns; read the word afterwards with device_error().  `flags`: an
+    optional int32 CUDA tensor of 2 elements, set to 0 where a wait gave up."""
+    import torch
+    if flags is not None and (not flags.is_cuda or flags.dtype != torch.int32 or flags.numel() < 2):
+        raise ValueError("flags must be an int32 CUDA tensor of at least 2 elements")
+    st = lib.oattn_selftest_wait(_ptr(flags), _stream(stream))
+    _raise(st, "oattn_selftest_wait")
 
 
 def device_error() -> int:

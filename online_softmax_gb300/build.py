@@ -16,7 +16,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "combine.cu", "decode.cu", "attn_fwd_d16.cu", "attn_fwd_d32.cu",
-           "attn_fwd_d64.cu", "attn_fwd_d128.cu", "mask.cu", "noalloc.cu"]
+           "attn_fwd_d64.cu", "attn_fwd_d128.cu", "mask.cu", "noalloc.cu", "selftest.cu"]
 
 
 def nvcc() -> str:

@@ -309,6 +309,15 @@ oattn_status oattn_device_error(int* code) {
   return v ? OATTN_ERR_TIMEOUT : OATTN_OK;
 }
 
+oattn_status oattn_selftest_wait(int* flags, struct CUstream_st* stream) {
+  if (flags != nullptr && !aligned(flags, 4)) return OATTN_ERR_INVALID_ARG;
+  cudaError_t e;
+  unsigned int* p = status_ptr(&e);
+  if (!p) return OATTN_ERR_CUDA;
+  return launch_selftest_wait(p, flags, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? OATTN_OK
+                                                                                               : OATTN_ERR_CUDA;
+}
+
 oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int N, int D, int causal, float scale, oattn_dtype dtype, int block_n,
                          struct CUstream_st* stream) {

@@ -17,6 +17,9 @@ cudaError_t launch_combine(const void* o_partial, const float* lse_partial, void
                            float* lse_out, int P, long long RH, int depth, int in_dt, int out_dt,
                            float lse_scale, bool pdl, cudaStream_t st);
 
+// ---- self-test of the bounded-wait failure path (selftest.cu)
+cudaError_t launch_selftest_wait(unsigned int* status, int* flags, cudaStream_t st);
+
 // ---- the optional Boolean mask, packed one bit per key (mask.cu packs it)
 // Row (b, h, q) of the mask starts at bits + b*sb + h*sh + q*sq (32-bit words; a stride
 // of 0 broadcasts); bit j of word w is key 32*w + j, set = visible.  A row holds
