@@ -22,7 +22,9 @@
  *     dense and row-major (last index contiguous).  16-bit and float32 tensors must start
  *     on a 16-byte boundary; float LSE arrays on a 4-byte boundary.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is enqueued
- *     and the call returns without synchronising.  Argument errors are returned before
+ *     and the call returns without synchronising.  The attention kernels are launched
+ *     as programmatic dependents of the previous kernel on the stream: they may be
+ *     scheduled while it finishes and wait for its completion before touching memory.  Argument errors are returned before
  *     anything is launched; a failed launch returns OATTN_ERR_CUDA.
  *   - Scores are s = scale * q.k.  Causal masking keeps key index <= query index (the
  *     diagonal included) and requires equal query and key lengths.

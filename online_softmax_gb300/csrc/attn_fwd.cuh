@@ -366,6 +366,11 @@ __global__ void __launch_bounds__(384, 1)
                     float scale_log2, int P, int chunk, int out_f32, const MaskArgs mk, const FusedMerge fm,
                     int ahead, unsigned int* status) {
   static_assert(!MASK || BN == 128, "the packed mask is read in 128-key tiles");
+  // Programmatic dependent launch: the next kernel on the stream may be scheduled once
+  // every CTA of this grid has started (its CTAs then take the SMs this grid's last
+  // wave frees); it waits for this grid's completion before touching memory, as this
+  // grid waits for the previous one below.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using C = AttnCfg<D, BN>;
   constexpr int BM = C::BM;
   constexpr int NSLOT = C::NSLOT;
@@ -439,6 +444,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar_done, 1);
     s_abort = 0;
     fence_mbar_init();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // previous grid done and visible
     if (nkv_max > 0) {
       mbar_arrive_expect_tx(&bar_q, (nkv0 > 0 ? C::Q_BYTES : 0) + (nkv1 > 0 ? C::Q_BYTES : 0));
       for (int t = 0; t < 2; ++t)
@@ -456,6 +462,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global access
   const uint32_t tmem = s_tmem;
   volatile int* abort = &s_abort;
 
@@ -801,9 +808,20 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   const long long blocks = npairs * a.BH * (a.P > 0 ? a.P : 1);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.BH,
-                                                           a.N, a.Nkv, a.causal, a.scale_log2, a.P, a.chunk,
-                                                           a.out_f32, a.mask, a.fused, sm_count(), a.status);
+  // Launched as a programmatic dependent of the previous kernel on the stream.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.BH, a.N, a.Nkv, a.causal,
+                         a.scale_log2, a.P, a.chunk, a.out_f32, a.mask, a.fused, sm_count(), a.status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
