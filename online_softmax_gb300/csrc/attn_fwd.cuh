@@ -350,6 +350,30 @@ __device__ __forceinline__ void merge_row(const void* o_partial, const float* ls
 }
 
 // 16 bytes of the packed mask (read-only path; rows of a shared mask stay in L2).
+// Key tiles marked in a bitmap (bit j of word j/32 = key tile j): how many of tiles
+// [0, n) are marked, and the first marked tile at or after `from` (callers walk at most
+// as many tiles as are marked; past the last word the walk returns the end index).
+constexpr int kNeedWords = 64;  // key tiles a CTA can skip over: 64 * 32 = 2048
+__device__ __forceinline__ int count_marked(const uint32_t* need, int n) {
+  int c = 0;
+  for (int w = 0; w * 32 < n; ++w) {
+    uint32_t bits = need[w];
+    if (n - w * 32 < 32) bits &= (1u << (n - w * 32)) - 1u;
+    c += __popc(bits);
+  }
+  return c;
+}
+__device__ __forceinline__ int next_marked(const uint32_t* need, int from) {
+  int w = from >> 5;
+  if (w >= kNeedWords) return kNeedWords * 32;
+  uint32_t bits = need[w] & (~0u << (from & 31));
+  while (bits == 0u) {
+    if (++w >= kNeedWords) return kNeedWords * 32;
+    bits = need[w];
+  }
+  return w * 32 + __ffs(bits) - 1;
+}
+
 __device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -381,6 +405,7 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_last;
+  __shared__ uint32_t s_need[MASK ? kNeedWords : 1];  // masked instances: key tiles to visit
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -419,8 +444,12 @@ __global__ void __launch_bounds__(384, 1)
     return key_end > kv_lo ? (key_end - kv_lo + BN - 1) / BN : 0;
   };
   const int row0_0 = pair * 2 * BM, row0_1 = row0_0 + BM;
-  const int nkv0 = tiles_for(row0_0), nkv1 = tiles_for(row0_1);
-  const int nkv_max = max(nkv0, nkv1);
+  const int nkv0_all = tiles_for(row0_0), nkv1_all = tiles_for(row0_1);
+  const int nkv_all = max(nkv0_all, nkv1_all);  // key tiles in range, before any skipping
+  // With the optional mask, key tiles that no row of this CTA sees are skipped by every
+  // role.  They are only known after the set-up, so only the first key tile (always
+  // visited) is loaded before it; its copy overlaps the scan of the mask.
+  const bool skip = MASK && nkv_all <= 32 * kNeedWords;
 
   // ---- set-up: barriers, TMEM
   if (warp == 9) {
@@ -429,7 +458,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   // The copy thread sets up the barriers and starts the copies of Q and of the first ring
   // of K/V tiles before the CTA-wide barrier, so they overlap the TMEM allocation.
-  const int first = min(NSLOT, 2 * nkv_max);  // K/V loads issued before the CTA barrier
+  const int first = min(skip ? 2 : NSLOT, 2 * nkv_all);  // K/V loads issued before the CTA barrier
   if (warp == 8 && lane == 0) {
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -442,13 +471,17 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_o[t], 1);
     }
     mbar_init(&bar_done, 1);
+    if constexpr (MASK) {
+      for (int i = 0; i < kNeedWords; ++i) s_need[i] = 0u;
+      if (skip && nkv_all > 0) s_need[0] = 1u;  // key tile 0: loaded before the scan
+    }
     s_abort = 0;
     fence_mbar_init();
     asm volatile("griddepcontrol.wait;" ::: "memory");  // previous grid done and visible
-    if (nkv_max > 0) {
-      mbar_arrive_expect_tx(&bar_q, (nkv0 > 0 ? C::Q_BYTES : 0) + (nkv1 > 0 ? C::Q_BYTES : 0));
+    if (nkv_all > 0) {
+      mbar_arrive_expect_tx(&bar_q, (nkv0_all > 0 ? C::Q_BYTES : 0) + (nkv1_all > 0 ? C::Q_BYTES : 0));
       for (int t = 0; t < 2; ++t)
-        if ((t ? nkv1 : nkv0) > 0)
+        if ((t ? nkv1_all : nkv0_all) > 0)
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? row0_1 : row0_0, bh);
       for (int n = 0; n < first; ++n) {  // the ring starts empty: no wait
@@ -466,12 +499,51 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = s_tmem;
   volatile int* abort = &s_abort;
 
+  // Masked instances: the softmax warps mark every key tile that some row of theirs
+  // sees (lane = key tile, one coalesced 512-byte load per row and 32 tiles; the rows a
+  // causal tile cannot reach are not looked at), then every role counts and walks the
+  // marked tiles only (tile 0 is always marked: it is already on its way).  A skipped
+  // tile has no visible key for any row of the CTA, so leaving it out changes no result.
+  int nkv0 = nkv0_all, nkv1 = nkv1_all;
+  if constexpr (MASK) {
+    if (skip) {
+      if (warp < 8) {
+        const int tt = warp >> 2;
+        const int rbase = (tt ? row0_1 : row0_0) + (warp & 3) * 32;
+        const int n_t = tt ? nkv1_all : nkv0_all;
+        const int b = bh / mk.H, h = bh - b * mk.H;
+        const uint32_t* base = mk.bits + b * mk.sb + h * mk.sh + (kv_lo >> 5);
+        for (int g = 0; g * 32 < n_t; ++g) {
+          const int j = g * 32 + lane;
+          uint32_t acc = 0u;
+#pragma unroll 1
+          for (int r0 = 0; r0 < 32; r0 += 16) {
+            uint4 w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int row = rbase + r0 + i;
+              w[i] = (j < n_t && row < N) ? ld_mask16(base + (long long)row * mk.sq + 4 * j) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc |= w[i].x | w[i].y | w[i].z | w[i].w;
+          }
+          const uint32_t marks = __ballot_sync(0xffffffffu, acc != 0u);
+          if (lane == 0 && marks != 0u) atomicOr(&s_need[g], marks);
+        }
+      }
+      __syncthreads();
+      nkv0 = count_marked(s_need, nkv0_all);
+      nkv1 = count_marked(s_need, nkv1_all);
+    }
+  }
+  const int nkv_max = max(nkv0, nkv1);
+
   // Registers move from the copy/MMA warpgroup to the softmax warpgroups.  Each
   // setmaxnreg sits at the top of its role's branch so that the register allocator
   // sees the new limit for all of that role's code.
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER));
-    if (warp == 8 && lane == 0 && nkv_max > 0) {
+    if (warp == 8 && lane == 0 && nkv_all > 0) {
       // ============================================================== TMA producer
       // Warm L2 with the Q tiles of the CTA `ahead` launches later (one wave on), which
       // is about when this SM or another picks it up: its first loads then hit L2.
@@ -483,13 +555,21 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < C::NCH; ++c) tma_prefetch_3d(&tm_q, c * C::CH, pair2 * 2 * BM + t * BM, bh2);
       }
       int issued = first;
+      int ktile = first > 0 ? 0 : -1;  // masked instances: the marked key tile of K/V load n
       for (int n = first; n < 2 * nkv_max; ++n) {
         const int slot = n % NSLOT;
         const uint32_t use = n / NSLOT;
         if (!mbar_wait(&bar_empty[slot], (use & 1u) ^ 1u, abort, status, kErrWaitLoad)) break;
         mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
         const CUtensorMap* map = (n & 1) ? &tm_v : &tm_k;
-        const int key0 = kv_lo + (n >> 1) * BN;
+        int tile_n = n >> 1;
+        if constexpr (MASK) {
+          if (skip) {
+            if ((n & 1) == 0) ktile = next_marked(s_need, ktile + 1);
+            tile_n = ktile;
+          }
+        }
+        const int key0 = kv_lo + tile_n * BN;
         uint8_t* dst = sKV + slot * C::KV_BYTES;
         for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * BN * C::SW, map, &bar_full[slot], c * C::CH, key0, bh);
         issued = n + 1;
@@ -580,10 +660,12 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     if (row0 < N) {
+      int tj = -1;  // key tile of iteration j (masked instances skip unmarked tiles)
       for (int j = 0; j < nkv; ++j) {
+        tj = (MASK && skip) ? next_marked(s_need, tj + 1) : j;
         uint4 w = make_uint4(~0u, ~0u, ~0u, ~0u);
         if constexpr (MASK) {
-          if (mrow != nullptr) w = ld_mask16(mrow + 4 * j);
+          if (mrow != nullptr) w = ld_mask16(mrow + 4 * tj);
         }
         ok = mbar_wait(&bar_s[t], (uint32_t)j & 1u, abort, status, kErrWaitS);
         ok = __all_sync(0xffffffffu, ok);
@@ -603,7 +685,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < BN; ++c) s[c] = ((ww[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
           }
         }
-        const int key0 = kv_lo + j * BN;
+        const int key0 = kv_lo + tj * BN;
         if ((key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0)) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) {
@@ -690,7 +772,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < D / W; ++c) {
             uint32_t u[W];
-            tmem_load_cols<W>(trow + col_o + c * W, u);
+            if (!MASK || nkv > 0) {
+              tmem_load_cols<W>(trow + col_o + c * W, u);
+            } else {  // every key tile of this query tile was skipped: o = +0
+#pragma unroll
+              for (int i = 0; i < W; ++i) u[i] = 0u;
+            }
             uint32_t w[W / 2];
 #pragma unroll
             for (int i = 0; i < W / 2; ++i)

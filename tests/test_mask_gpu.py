@@ -170,6 +170,49 @@ def test_fully_hidden_problem():
     assert dead == 2 * 130
 
 
+# ------------------------------------------------------------------ skipped key tiles
+def skip_masks(N):
+    """Masks whose key tiles are invisible to whole CTAs (256 query rows) or whole query
+    tiles (128 rows), so the masked kernel walks only part of the key range."""
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    out = {}
+    out["window 100"] = synth.mask_band(N, N, 100)
+    # rows 0-127 see nothing; rows 128-255 only keys 128-255; the rest a 300-key window
+    m = synth.mask_band(N, N, 300)
+    m[:128] = False
+    m[128:256] = (j >= 128) & (j < 256)
+    out["first tile hidden"] = m
+    # one whole CTA (rows 256-511) sees nothing; key tiles 0 and 5 only for the others
+    m = ((j // 128) == 0) | ((j // 128) == 5)
+    m = np.broadcast_to(m, (N, N)).copy()
+    m[256:512] = False
+    out["CTA hidden, tiles 0 and 5"] = m
+    # short key padding: keys 0-99 only
+    out["keys 0-99"] = np.broadcast_to(j < 100, (N, N)).copy()
+    return out
+
+
+@pytest.mark.parametrize("name", ["window 100", "first tile hidden", "CTA hidden, tiles 0 and 5", "keys 0-99"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_masked_tiles_skipped(name, causal, D):
+    N = 1100
+    qb, kb, vb = H.qkv_host(200 + D, 1, 2, N, D, "bf16")
+    mask = skip_masks(N)[name]
+    dead = check_masked(qb, kb, vb, "bf16", mask, causal, f"{name} D{D} c{causal}")
+    if name in ("first tile hidden", "CTA hidden, tiles 0 and 5"):
+        assert dead > 0  # the recipe hides whole query tiles; make sure they are exercised
+
+
+def test_masked_tiles_skipped_split_k():
+    N = 1100
+    qb, kb, vb = H.qkv_host(210, 1, 2, N, 128, "bf16")
+    for name, mask in skip_masks(N).items():
+        for causal in (False, True):
+            check_splitk_masked(qb, kb, vb, "bf16", 3, mask, causal, "f32", f"split {name} c{causal}")
+
+
 # ------------------------------------------------------------------ split-K
 def run_splitk_masked(q, k, v, P, mask, causal, partial="f32"):
     B, Hh, Nq, D = q.shape
