@@ -243,3 +243,15 @@ def test_attn_fwd_host_rejects(lib, kw, expect):
 
 def test_attn_fwd_host_empty(lib):
     assert host(lib, qh=None, kh=None, vh=None, oh=None, qd=None, kd=None, vd=None, od=None, N=0) == 0
+
+
+def test_selftest_site_code_matches_binding():
+    """The site code the self-test records is the one the header documents and the
+    binding compares against."""
+    import online_softmax_gb300 as ops
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+OATTN_SELFTEST_SITE\s+(0x[0-9A-Fa-f]+)", text)
+    assert m is not None
+    assert int(m.group(1), 16) == ops.SELFTEST_SITE
+    src = open(os.path.join(ROOT, "online_softmax_gb300", "csrc", "selftest.cu")).read()
+    assert re.search(r"kErrSelfTest\s*=\s*" + m.group(1), src)
