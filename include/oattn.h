@@ -77,8 +77,8 @@ typedef enum { OATTN_F16 = 0, OATTN_BF16 = 1, OATTN_F32 = 2 } oattn_dtype;
  * or OATTN_ERR_CUDA.
  */
 OATTN_API oattn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                      int B, int H, int N, int D, int causal, float scale,
-                      oattn_dtype dtype, struct CUstream_st* stream);
+                                int B, int H, int N, int D, int causal, float scale,
+                                oattn_dtype dtype, struct CUstream_st* stream);
 
 /*
  * attn_fwd_host - attn_fwd with the inputs and outputs in HOST memory: the heads are cut
@@ -100,9 +100,9 @@ OATTN_API oattn_status attn_fwd(const void* q, const void* k, const void* v, voi
  * must not alias.  Errors as attn_fwd.
  */
 OATTN_API oattn_status attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
-                           float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d,
-                           float* lse_d, int B, int H, int N, int D, int causal, float scale,
-                           oattn_dtype dtype, int chunk_heads, struct CUstream_st* stream);
+                                     float* lse_h, void* q_d, void* k_d, void* v_d, void* o_d,
+                                     float* lse_d, int B, int H, int N, int D, int causal, float scale,
+                                     oattn_dtype dtype, int chunk_heads, struct CUstream_st* stream);
 
 /*
  * attn_fwd_bn - attn_fwd with an explicit key-tile width block_n in {32, 64, 128}
@@ -111,8 +111,8 @@ OATTN_API oattn_status attn_fwd_host(const void* q_h, const void* k_h, const voi
  * only by floating-point summation order.
  */
 OATTN_API oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, void* o, float* lse,
-                         int B, int H, int N, int D, int causal, float scale,
-                         oattn_dtype dtype, int block_n, struct CUstream_st* stream);
+                                   int B, int H, int N, int D, int causal, float scale,
+                                   oattn_dtype dtype, int block_n, struct CUstream_st* stream);
 
 /*
  * attn_fwd_splitk - attention with the key axis split into P partitions.
@@ -134,9 +134,9 @@ OATTN_API oattn_status attn_fwd_bn(const void* q, const void* k, const void* v, 
  * o or lse.
  */
 OATTN_API oattn_status attn_fwd_splitk(const void* q, const void* k, const void* v, void* o, float* lse,
-                             int B, int H, int Nq, int Nkv, int D, int causal, float scale,
-                             oattn_dtype dtype, int P, void* o_partial, float* lse_partial,
-                             oattn_dtype partial_dtype, struct CUstream_st* stream);
+                                       int B, int H, int Nq, int Nkv, int D, int causal, float scale,
+                                       oattn_dtype dtype, int P, void* o_partial, float* lse_partial,
+                                       oattn_dtype partial_dtype, struct CUstream_st* stream);
 
 /*
  * splitk_combine - merge P partitions by their base-2 LSEs ("fa4_splitk_combine").
@@ -154,9 +154,9 @@ OATTN_API oattn_status attn_fwd_splitk(const void* q, const void* k, const void*
  *   between 32 and 1024 bytes (f32: 8..256, f16/bf16: 16..512).
  */
 OATTN_API oattn_status splitk_combine(const void* o_partial, const float* lse_partial, void* o,
-                            float* lse_out, int P, int rows, int heads, int depth,
-                            oattn_dtype in_dtype, oattn_dtype out_dtype,
-                            struct CUstream_st* stream);
+                                      float* lse_out, int P, int rows, int heads, int depth,
+                                      oattn_dtype in_dtype, oattn_dtype out_dtype,
+                                      struct CUstream_st* stream);
 
 /*
  * attn_fwd_splitk_noalloc - attn_fwd_splitk for callers that cannot allocate device
@@ -178,8 +178,8 @@ OATTN_API oattn_status splitk_combine(const void* o_partial, const float* lse_pa
  *   the caller.  Each call rewrites every partial it reads, so no clearing is needed.
  */
 OATTN_API oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
-                                     int B, int H, int Nq, int Nkv, int D, int causal, float scale,
-                                     oattn_dtype dtype, int P, struct CUstream_st* stream);
+                                               int B, int H, int Nq, int Nkv, int D, int causal, float scale,
+                                               oattn_dtype dtype, int P, struct CUstream_st* stream);
 
 /*
  * The optional Boolean M x N mask ("Streaming attention and online state", section
@@ -213,18 +213,20 @@ OATTN_API int attn_mask_words(int Nkv);
  * null or misaligned pointers or row_stride < Nkv.
  */
 OATTN_API oattn_status attn_mask_pack(const void* mask, unsigned int* bits, long long rows, int Nkv,
-                            long long row_stride, struct CUstream_st* stream);
+                                      long long row_stride, struct CUstream_st* stream);
 
 /*
  * attn_fwd_masked - attn_fwd (key tiles of 128) with the optional Boolean mask added.
  *   Arguments as attn_fwd, plus the packed mask and its strides (above); the mask is
- *   required (non-NULL) when N > 0.  Causal and mask may be combined.
+ *   required (non-NULL) when N > 0.  Causal and mask may be combined.  Key tiles that
+ *   no row of a block of 256 query rows sees are skipped, so a sliding window or key
+ *   padding costs only the tiles it touches (the mask is scanned once per block).
  */
 OATTN_API oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
-                             int B, int H, int N, int D, int causal, float scale,
-                             oattn_dtype dtype, const unsigned int* mask_bits,
-                             long long mask_stride_b, long long mask_stride_h,
-                             long long mask_stride_q, struct CUstream_st* stream);
+                                       int B, int H, int N, int D, int causal, float scale,
+                                       oattn_dtype dtype, const unsigned int* mask_bits,
+                                       long long mask_stride_b, long long mask_stride_h,
+                                       long long mask_stride_q, struct CUstream_st* stream);
 
 /*
  * attn_fwd_splitk_masked - attn_fwd_splitk with the optional Boolean mask (above) over
@@ -233,12 +235,12 @@ OATTN_API oattn_status attn_fwd_masked(const void* q, const void* k, const void*
  *   row q = 0 of each (b, h), so mask_stride_q is not used there.
  */
 OATTN_API oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v, void* o,
-                                    float* lse, int B, int H, int Nq, int Nkv, int D,
-                                    int causal, float scale, oattn_dtype dtype, int P,
-                                    void* o_partial, float* lse_partial,
-                                    oattn_dtype partial_dtype, const unsigned int* mask_bits,
-                                    long long mask_stride_b, long long mask_stride_h,
-                                    long long mask_stride_q, struct CUstream_st* stream);
+                                              float* lse, int B, int H, int Nq, int Nkv, int D,
+                                              int causal, float scale, oattn_dtype dtype, int P,
+                                              void* o_partial, float* lse_partial,
+                                              oattn_dtype partial_dtype, const unsigned int* mask_bits,
+                                              long long mask_stride_b, long long mask_stride_h,
+                                              long long mask_stride_q, struct CUstream_st* stream);
 
 /*
  * attn_fwd_splitk_fused - attn_fwd_splitk with the merge done inside the attention
@@ -264,13 +266,13 @@ OATTN_API oattn_status attn_fwd_splitk_masked(const void* q, const void* k, cons
 OATTN_API int attn_splitk_counters(int B, int H, int Nq);
 
 OATTN_API oattn_status attn_fwd_splitk_fused(const void* q, const void* k, const void* v, void* o,
-                                   float* lse, int B, int H, int Nq, int Nkv, int D,
-                                   int causal, float scale, oattn_dtype dtype, int P,
-                                   void* o_partial, float* lse_partial,
-                                   oattn_dtype partial_dtype, unsigned int* counters,
-                                   const unsigned int* mask_bits, long long mask_stride_b,
-                                   long long mask_stride_h, long long mask_stride_q,
-                                   struct CUstream_st* stream);
+                                             float* lse, int B, int H, int Nq, int Nkv, int D,
+                                             int causal, float scale, oattn_dtype dtype, int P,
+                                             void* o_partial, float* lse_partial,
+                                             oattn_dtype partial_dtype, unsigned int* counters,
+                                             const unsigned int* mask_bits, long long mask_stride_b,
+                                             long long mask_stride_h, long long mask_stride_q,
+                                             struct CUstream_st* stream);
 
 /* Key chunk per partition used by attn_fwd_splitk (host-only, no GPU needed). */
 OATTN_API int splitk_chunk(int Nkv, int P);
