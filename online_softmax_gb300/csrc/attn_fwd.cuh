@@ -26,9 +26,9 @@
 //     Keys past the end of the sequence arrive as zeros (out-of-bounds fill).
 //   * S_t = Q_t K^T is a kind::f16 MMA (M=128, N=BN, K=D) into TMEM columns
 //     [t*BN, (t+1)*BN).  The softmax threads read their row (tcgen05.ld), mask with
-//     -inf, take the max, compute p = 2^(s*scale*log2e - m) with one FMA and one
-//     ex2.approx each, sum the FP32 p, round p to the input dtype (cvt.rn, round to
-//     nearest even) and write it back over S (tcgen05.st) as the A operand of
+//     -inf, compute p = 2^(s*scale*log2e - m) with one FMA and one ex2.approx each (in
+//     chunks of 64 columns), sum the FP32 p, round p to the input dtype (cvt.rn, round
+//     to nearest even) and write it back over S (tcgen05.st) as the A operand of
 //     O_t += P V (M=128, N=D, K=BN, A from TMEM, B = V tile read MN-major).
 //   * The single MMA-issuing thread is the critical path: each mbarrier wait it makes
 //     costs it ~150-200 cycles while the tensor pipe streams shared memory, even when
@@ -52,11 +52,17 @@
 //   * The optional Boolean M x N mask ("Streaming attention and online state", section
 //     "Attention as a consumer") arrives packed one bit per key: each softmax thread
 //     reads the 16 bytes of its row that cover the key tile while it waits for the
-//     tile's scores, and turns the hidden scores to -inf with selects; a warp whose 32 rows see the whole tile
-//     skips the selects.
+//     tile's scores, and turns the hidden scores to -inf with selects; a warp whose 32
+//     rows see the whole tile skips the selects.  Before the key loop the softmax warps
+//     scan the mask once and mark the key tiles that some row of the CTA sees; every
+//     role then walks the marked tiles only (key tile 0 is always visited).
 //   * CTAs are ordered in groups of kHeadGroup heads: within a group the query-tile
 //     pairs run longest first (causal), and the few heads in flight keep their K/V in
 //     L2 instead of streaming every head's K/V from HBM for every pair.
+//
+//   * Launches are programmatic dependents of the previous kernel on the stream: every
+//     CTA lets the next grid be scheduled as soon as it starts, and waits for the
+//     previous grid (griddepcontrol.wait) before its first global access.
 //
 // Every wait is bounded (see ptx.cuh); a thread that gives up marks the CTA aborted,
 // everyone leaves its loop, copies and MMAs in flight are drained, TMEM is freed.
