@@ -62,3 +62,30 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
         steps, warmup, gpus = 1, 3, 2
     bench.run_reference(A())
     assert capsys.readouterr().out == ""
+
+
+def test_profiled_traffic_follows_the_kernel_code_not_its_comments(tmp_path, monkeypatch):
+    """The bench attaches the committed DRAM counters only while the profiled kernel code
+    is unchanged: a comment edit keeps them, a code edit retires them."""
+    sys.path.insert(0, ROOT)
+    import shutil
+    import bench
+    srcs = []
+    for rel in bench.KERNEL_SOURCES:
+        dst = tmp_path / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(ROOT, rel), dst)
+        srcs.append(dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    prof = tmp_path / "profiles" / "kernel.md"
+    prof.parent.mkdir(parents=True, exist_ok=True)
+    prof.write_text(f"# capture\n\n- kernel_source_sha256_16: `{bench.kernel_source_hash()}`\n"
+                    "- dram_bytes_per_launch: `123456`\n")
+    monkeypatch.setattr(bench, "PROFILE", str(prof))
+    assert bench.profiled_traffic() == 123456.0
+    with open(srcs[0], "a") as f:
+        f.write("\n// a comment added after the capture\n")
+    assert bench.profiled_traffic() is not None
+    with open(srcs[0], "a") as f:
+        f.write("\nnamespace oattn { constexpr int kAddedAfterCapture = 1; }\n")
+    assert bench.profiled_traffic() is None
