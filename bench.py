@@ -6,10 +6,15 @@ larger than L2).  Rank 0 prints one JSON line:
   value     whole-job attention TFLOP/s (algorithmic causal FLOPs 4*B*H*D*N(N+1)/2)
   e2e       the same metric through the public API with pinned host buffers and the
             host<->device copies inside the timed region
-  roofline  the attention kernel against the measured dense BF16 peak
+  roofline  the attention kernel against the measured dense BF16 peak, and against
+            peaks that account for the SM clock sampled during the timed region
+  clocks    SM clock and throttle reasons sampled in-process (NVML, ~1 ms) during it
+  noncausal the same inputs without the causal rule
   combine   split-K LSE combine GB/s on 4096x32 row-heads, depth 128, P in {2,8,16,32,37}
-  decode_splitk  split-K decode (64 x 32 heads, 32768 keys) + combine, GB/s
-  cpu_baseline   the FP64 oracle on the host cores, on a bounded sample
+  decode_splitk  split-K decode (64 x 32 heads, 32768 keys) + combine, GB/s; PDL
+            against separate calls where the combine is a visible share (P = 37, 148)
+  cpu_baseline   the FP64 oracle on the host cores, on a bounded sample (also inside
+            the combine and decode objects, for those legs)
 With --impl reference the FP64 oracle itself is timed (host cores) on samples of
 the same workload.
 
@@ -39,6 +44,10 @@ SEED = 3
 FLOPS = 4.0 * B * H * D * N * (N + 1) / 2  # algorithmic causal FLOPs per step
 WORKLOAD = "prefill attention forward B=4 H=32 N=4096 D=128 bf16 causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's published HBM3e bandwidth of one GB300 GPU (8 TB/s).  The measured peak
+# (MEASURED_PEAKS.json) is a read+write copy, which read-dominated kernels can beat;
+# fractions against this figure are reported beside it.
+DATASHEET_HBM_GBS = 8000.0
 PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_prefill_b4h32n4096d128.md")
 KERNEL_SOURCES = ["online_softmax_gb300/csrc/attn_fwd.cuh", "online_softmax_gb300/csrc/ptx.cuh",
                   "online_softmax_gb300/csrc/tmem_regs.cuh"]
@@ -108,18 +117,74 @@ def profiled_traffic():
         return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (clocks, clock-event reasons, power); None
+    when the library or the device cannot be opened.  Nothing here sets anything."""
+    SM_CLOCK = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, pci_bus_id: str | None, index: int):
+        import ctypes
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        if self.lib.nvmlInit_v2() != 0:
+            return
+        self.h = ctypes.c_void_p()
+        rc = -1
+        if pci_bus_id:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        self.ok = rc == 0
+        self.ctypes = ctypes
+
+    def sm_mhz(self):
+        v = self.ctypes.c_uint(0)
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM_CLOCK, self.ctypes.byref(v)) == 0 else None
+
+    def sm_max_mhz(self):
+        v = self.ctypes.c_uint(0)
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM_CLOCK, self.ctypes.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = self.ctypes.c_ulonglong(0)
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        if fn is None or fn(self.h, self.ctypes.byref(v)) != 0:
+            return None
+        return [n for bit, n in self.REASONS.items() if v.value & bit]
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """SM clock and throttle reasons sampled every ~1 ms while the timed region runs,
+    with in-process NVML queries (read-only), so that a region of a few milliseconds
+    still gets samples; falls back to nvidia-smi at 100 ms when NVML cannot be opened."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, pci_bus_id: str | None = None, period_s: float = 0.001):
         self.gpu = gpu_index
+        self.pci = pci_bus_id
+        self.period = period_s
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.stamped, self.smax = [], None
+        self.t_start, self.t_end = None, None
+        self._stop = threading.Event()
 
     def __enter__(self):
+        self.nvml = _Nvml(self.pci, self.gpu)
+        if self.nvml.ok:
+            self.smax = self.nvml.sm_max_mhz()
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
+        self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
@@ -130,11 +195,29 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def mark(self, start: bool):
+        """Host time at which the timed region starts / ends: only samples taken
+        between the two count (the poller starts a little before the region)."""
+        if start:
+            self.t_start = time.perf_counter()
+        else:
+            self.t_end = time.perf_counter()
+
+    def _poll(self):
+        while not self._stop.is_set():
+            mhz = self.nvml.sm_mhz()
+            r = self.nvml.reasons()
+            self.stamped.append((time.perf_counter(), mhz, r))
+            time.sleep(self.period)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self._stop.set()
+        if self.nvml is not None:
+            self.t.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -143,7 +226,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons = [], self.smax, set()
+        for t, mhz, r in self.stamped:
+            if (self.t_start is not None and t < self.t_start) or (self.t_end is not None and t > self.t_end):
+                continue
+            if mhz is not None:
+                sm.append(float(mhz))
+            if r:
+                reasons.update(r)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -158,7 +248,8 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvml in-process, ~1 ms" if self.nvml is not None else "nvidia-smi, 100 ms"}
 
 
 # ---------------------------------------------------------------- oracle baseline
@@ -267,13 +358,14 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
     if args.part in ("all", "attn"):
         line.update(measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank))
+    cpu = rank == 0 and args.part == "all" and not args.no_cpu_baseline
     if args.part in ("all", "combine"):
         line["combine"] = measure_combine(torch, ops, sc, synth, pk, dev,
                                           [int(x) for x in args.combine_P.split(",")],
-                                          args.combine_dtype.split(","))
+                                          args.combine_dtype.split(","), cpu)
     if args.part in ("all", "decode"):
         line["decode_splitk"] = measure_decode(torch, ops, sc, synth, pk, dev, args.decode_batch,
-                                               [int(x) for x in args.decode_P.split(",")])
+                                               [int(x) for x in args.decode_P.split(",")], cpu)
     torch.cuda.empty_cache()
     if rank == 0 and args.part == "all" and not args.no_cpu_baseline:
         tf, secs, heads = oracle_sample(12.0)
@@ -306,15 +398,17 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
         step()
     torch.cuda.synchronize()
     barrier(world)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index, pci_bus_id(torch, dev)) as clk:
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clk.mark(True)
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(False)
         barrier(world)
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, world, dev)
@@ -323,6 +417,7 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
     per_launch_s = ms / 1e3 / args.steps
     achieved = FLOPS / per_launch_s / 1e12
     traffic = profiled_traffic()
+    clocks = clk.summary()
     line = {
         "value": value, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
@@ -330,16 +425,73 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
                    "parallelism": "replicas" if world == 1 else f"replicas x{world} (independent batches)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
-                     "peak_source": f"{pk_kind} (dense bf16 burst)", "kernel": "attn_fwd_kernel<128,128,bf16>"},
+                     "peak_source": f"{pk_kind} (dense bf16 burst)", "kernel": "attn_fwd_kernel<128,128,bf16>",
+                     **clock_aware_roofline(torch, dev, achieved, pk, clocks)},
         "gpu_launches": args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    line["noncausal"] = measure_noncausal(torch, ops, q, k, v, pk)
 
     if args.part == "all":
         line["e2e"] = measure_e2e(torch, ops, q, k, v, args, world, dev)
         line["context"] = measure_sdpa(torch, q, k, v)
         line["masked"] = measure_masked(torch, ops, synth, q, k, v, dev)
     return line
+
+
+def pci_bus_id(torch, dev):
+    """NVML's PCI bus id string of a torch device (None if torch does not expose it)."""
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except AttributeError:
+        return None
+
+
+# Dense bf16 tensor-core work one SM retires per SM clock: one kind::f16 MMA of
+# M=128, N=128, K=16 (2*128*128*16 FLOP) per 64 cycles, the back-to-back rate measured
+# on this part with operands resident in shared memory.
+FLOP_PER_SM_CLOCK = 2 * 128 * 128 * 16 / 64
+
+
+def clock_aware_roofline(torch, dev, achieved, pk, clocks):
+    """The attention rate against peaks that account for the SM clock.  The measured
+    cuBLAS peak was taken at the power-capped clock recorded beside it (median under
+    load), while this kernel runs at the clock sampled during its timed region:
+      frac_clock_scaled = achieved * (peak run's MHz / kernel's MHz) / measured peak
+      frac_of_clock_peak = achieved / (SMs * FLOP_PER_SM_CLOCK * kernel's MHz)."""
+    out = {}
+    mhz = clocks.get("sm_mhz")
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_mhz = float(json.load(f)["clocks_under_load"]["sm_mhz_median"])
+    except (OSError, KeyError, ValueError, TypeError):
+        peak_mhz = None
+    if mhz:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        at_clock = sms * FLOP_PER_SM_CLOCK * mhz * 1e6 / 1e12
+        out["kernel_sm_mhz"] = mhz
+        out["peak_at_kernel_clock"] = at_clock
+        out["frac_of_clock_peak"] = achieved / at_clock
+        if peak_mhz:
+            out["peak_run_sm_mhz"] = peak_mhz
+            out["frac_clock_scaled"] = achieved * (peak_mhz / mhz) / pk["bf16_tflops"]
+    return out
+
+
+def measure_noncausal(torch, ops, q, k, v, pk):
+    """The same inputs without the causal rule (every query sees every key)."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fn = lambda: ops.attn_fwd(q, k, v, o, lse, causal=False)
+    for _ in range(3):
+        fn()
+    med, _ = time_launches(torch, fn, 20)
+    flops = 4.0 * B * H * D * N * N
+    assert ops.device_error() == 0
+    return {"workload": "prefill attention forward B=4 H=32 N=4096 D=128 bf16 non-causal",
+            "flops_per_step": flops, "tflops": flops / med / 1e12, "ms": med * 1e3,
+            "frac": flops / med / 1e12 / pk["bf16_tflops"]}
 
 
 def measure_masked(torch, ops, synth, q, k, v, dev):
@@ -444,7 +596,7 @@ def time_launches(torch, fn, iters, flush=None):
     return statistics.median(ts), sum(ts) / len(ts)
 
 
-def measure_combine(torch, ops, sc, synth, pk, dev, Ps, dtypes):
+def measure_combine(torch, ops, sc, synth, pk, dev, Ps, dtypes, cpu=False):
     rows, heads, depth = 4096, 32, 128
     RH = rows * heads
     l2buf = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev)  # 512 MB
@@ -466,7 +618,7 @@ def measure_combine(torch, ops, sc, synth, pk, dev, Ps, dtypes):
             nbytes = P * RH * depth * esz + P * RH * 4 + RH * depth * esz + RH * 4
             gbs = nbytes / med / 1e9
             r = {"P": P, "dtype": dt, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs,
-                 "frac": gbs / pk["hbm_gbs"]}
+                 "frac": gbs / pk["hbm_gbs"], "frac_datasheet": gbs / DATASHEET_HBM_GBS}
             out["results"].append(r)
             if best is None or r["frac"] > best["frac"]:
                 best = r
@@ -474,12 +626,45 @@ def measure_combine(torch, ops, sc, synth, pk, dev, Ps, dtypes):
     assert ops.device_error() == 0
     del l2buf
     fr = [r["frac"] for r in out["results"]]
+    fd = [r["frac_datasheet"] for r in out["results"]]
     out["roofline"] = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
-                       "frac_min": min(fr), "frac_median": statistics.median(fr), "frac_max": max(fr)}
+                       "frac_min": min(fr), "frac_median": statistics.median(fr), "frac_max": max(fr),
+                       "datasheet_peak": DATASHEET_HBM_GBS, "frac_datasheet_min": min(fd),
+                       "frac_datasheet_max": max(fd),
+                       "below_0.70_of_datasheet": [f"{r['dtype']} P={r['P']}" for r in out["results"]
+                                                   if r["frac_datasheet"] < 0.70]}
+    if cpu:
+        out["cpu_baseline"] = combine_cpu_baseline(6.0)
     return out
 
 
-def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps):
+def combine_cpu_baseline(budget_s: float):
+    """The FP64 oracle's combine on the host cores: the first 2048 row-heads of the f32
+    P = 16 workload, combined again and again until `budget_s` of CPU work has run; GB/s
+    of the same algorithmic bytes the GPU number counts."""
+    import numpy as np
+    import oracle
+    import synth
+    rows, heads, depth, P, n = 4096, 32, 128, 16, 2048
+    RH = rows * heads
+    lse = synth.lse_partials(21, P, RH, 0, n).astype(np.float64)
+    # partition p's first n row-heads are one contiguous run of the generator's stream
+    op = np.stack([synth.normal(21, synth.STREAM_OPART, p * RH * depth, n * depth).reshape(n, depth)
+                   for p in range(P)]).astype(np.float64)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps == 0:
+        t0 = time.perf_counter()
+        oracle.combine(op, lse)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    done = reps * n
+    nbytes = P * done * depth * 4 + P * done * 4 + done * depth * 4 + done * 4
+    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"the first {n} row-heads of the f32 P=16 workload, combined {reps} times by the FP64 "
+                      f"numpy oracle, {t_total:.1f} s"}
+
+
+def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps, cpu=False):
     Hd, Nkv, Dd = 32, 32768, 128
     q = sc.fill_normal(torch.empty((Bd, Hd, 1, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_Q, "bf16")
     k = sc.fill_normal(torch.empty((Bd, Hd, Nkv, Dd), dtype=torch.bfloat16, device=dev), 5, synth.STREAM_K, "bf16")
@@ -509,6 +694,7 @@ def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps):
         nbytes = 2 * Bd * Hd * Nkv * Dd * 2 + q.numel() * 2 + 2 * (P * RH * Dd * 4 + P * RH * 4) + o.numel() * 2
         gbs = nbytes / med / 1e9
         out["results"].append({"P": P, "bytes": nbytes, "us": med * 1e6, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"],
+                               "frac_datasheet": gbs / DATASHEET_HBM_GBS,
                                "us_separate_calls": med_sep * 1e6, "pdl_speedup": med_sep / med,
                                "us_fused_merge": med_fused * 1e6, "fused_speedup": med / med_fused})
     # one sequence: the merge is a larger share of a short step
@@ -528,12 +714,69 @@ def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps):
         small.append({"P": P, "us": med * 1e6, "us_fused_merge": med_fused * 1e6, "fused_speedup": med / med_fused})
     out["one_sequence"] = {"workload": "1 sequence x 1 query, 32 heads, 32768 keys, D=128, bf16",
                            "results": small}
+    # PDL where the combine is a visible share of the step ("fa4_splitk_combine", PDL
+    # paragraph, measured 1.06-1.13x on P = 148 combine-heavy shapes on SM100): one
+    # sequence, many partitions; the producer + PDL combine of attn_fwd_splitk against the
+    # same two kernels as separate calls in plain stream order.
+    heavy = []
+    for P in (37, 148):
+        q1, k1, v1 = q[:1], k[:1], v[:1]
+        op = torch.empty((P, Hd, Dd), dtype=torch.float32, device=dev)
+        lp = torch.empty((P, Hd), dtype=torch.float32, device=dev)
+        o1 = torch.empty_like(q1)
+        fn = lambda: ops.attn_fwd_splitk(q1, k1, v1, P, op, lp, o1, None)
+        fn_sep = lambda: (ops.attn_fwd_splitk(q1, k1, v1, P, op, lp, None, None),
+                          ops.splitk_combine(op, lp, o1.view(Hd, Dd), rows=1, heads=Hd))
+        for _ in range(3):
+            fn()
+            fn_sep()
+        meds, seps = [], []
+        for _ in range(5):  # interleaved rounds, so that drifting clocks hit both alike
+            meds.append(time_launches(torch, fn, 20)[0])
+            seps.append(time_launches(torch, fn_sep, 20)[0])
+        med, med_sep = statistics.median(meds), statistics.median(seps)
+        heavy.append({"P": P, "us_pdl": med * 1e6, "us_separate_calls": med_sep * 1e6, "pdl_speedup": med_sep / med})
+    out["pdl_combine_heavy"] = {"workload": "1 sequence x 1 query, 32 heads, 32768 keys, D=128, bf16, P in {37, 148}",
+                                "results": heavy}
     assert ops.device_error() == 0
     fr = [r["frac"] for r in out["results"]]
+    fd = [r["frac_datasheet"] for r in out["results"]]
     out["roofline"] = {"bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s", "frac_min": min(fr),
-                       "frac_max": max(fr)}
+                       "frac_max": max(fr), "datasheet_peak": DATASHEET_HBM_GBS,
+                       "frac_datasheet_min": min(fd), "frac_datasheet_max": max(fd)}
     del q, k, v
+    if cpu:
+        out["cpu_baseline"] = decode_cpu_baseline(6.0, Ps)
     return out
+
+
+def decode_cpu_baseline(budget_s: float, Ps):
+    """The FP64 oracle on decode row-heads of the workload (one query against 32768 keys,
+    D=128): the split-K partials for the largest P of the run plus their combine, on the
+    first two row-heads again and again until `budget_s` of CPU work has run; GB/s of the
+    K/V bytes those row-heads read (bf16), the bytes the GPU number is dominated by."""
+    import numpy as np
+    import oracle
+    import synth
+    from tests import helpers as Hl
+    Nkv, Dd, seed = 32768, 128, 5
+    P = max(Ps)
+    bounds = oracle.splitk_bounds(Nkv, P, 128)
+    scale = 1.0 / math.sqrt(Dd)
+    heads = [tuple(Hl.head_slice(seed, st, bh, n, Dd, "bf16") for st, n in
+                   ((synth.STREAM_Q, 1), (synth.STREAM_K, Nkv), (synth.STREAM_V, Nkv))) for bh in (0, 1)]
+    done, t_total = 0, 0.0
+    while t_total < budget_s or done == 0:
+        qr, kh, vh = heads[done % 2]
+        t0 = time.perf_counter()
+        Op, Lp = oracle.splitk_partials_rows(qr, np.array([0]), kh, vh, scale, False, bounds)
+        oracle.combine(Op, Lp)
+        t_total += time.perf_counter() - t0
+        done += 1
+    nbytes = done * 2 * Nkv * Dd * 2
+    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"row-heads 0 and 1 of the decode workload, {done} oracle runs (P={P} partials + combine), "
+                      f"FP64 numpy oracle, {t_total:.1f} s"}
 
 
 if __name__ == "__main__":

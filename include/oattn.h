@@ -168,9 +168,11 @@ OATTN_API oattn_status splitk_combine(const void* o_partial, const float* lse_pa
  *   Arguments as attn_fwd_splitk, without o_partial / lse_partial / partial_dtype: the
  *   float32 partials go to a fixed workspace inside the library (a device array of
  *   10 Mi + 256 Ki floats, 41 MiB, held on every GPU that loads the library until the
- *   process exits).  o is required; lse may be NULL.
+ *   process exits).  o is required when Nq > 0; lse may be NULL.
  *   Requires P * B*H*Nq * D <= 10485760 and P * B*H*Nq <= 262144, else returns
- *   OATTN_ERR_UNSUPPORTED before touching the device.  Other errors as attn_fwd_splitk.
+ *   OATTN_ERR_UNSUPPORTED before touching the device.  Every other argument is checked
+ *   as attn_fwd_splitk checks it, empty problems (Nq == 0) included, with the same
+ *   errors.
  *   The first call on a device looks up the workspace's device address (a host-side
  *   runtime call); make that first call before any stream capture.
  *   Every call uses the same workspace: calls that may overlap on the GPU (different

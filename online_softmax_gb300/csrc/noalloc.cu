@@ -56,15 +56,17 @@ extern "C" oattn_status attn_fwd_splitk_noalloc(const void* q, const void* k, co
                                                 float* lse, int B, int H, int Nq, int Nkv, int D,
                                                 int causal, float scale, oattn_dtype dtype, int P,
                                                 struct CUstream_st* stream) {
-  if (!o) return OATTN_ERR_INVALID_ARG;  // the merged output is the only result
+  if (Nq > 0 && !o) return OATTN_ERR_INVALID_ARG;  // the merged output is the only result
   if (B < 1 || H < 1 || Nq < 0 || P < 1) return OATTN_ERR_INVALID_ARG;
   const long long rows = (long long)B * H * Nq;
   if ((long long)P * rows * D > kNoallocPartialFloats || (long long)P * rows > kNoallocLseFloats)
     return OATTN_ERR_UNSUPPORTED;  // beyond the fixed workspace
-  if (Nq == 0) return OATTN_OK;
+  // An empty problem still goes through attn_fwd_splitk, which checks every other
+  // argument (dtype, D, scale, P) and then returns without touching the device; the
+  // workspace address is only looked up when there is work.
   float* partial = nullptr;
   float* lse_partial = nullptr;
-  if (!noalloc_scratch(&partial, &lse_partial)) return OATTN_ERR_CUDA;
+  if (Nq > 0 && !noalloc_scratch(&partial, &lse_partial)) return OATTN_ERR_CUDA;
   // Every partition row is rewritten by each call, so nothing needs clearing first.
   return attn_fwd_splitk(q, k, v, o, lse, B, H, Nq, Nkv, D, causal, scale, dtype, P, partial, lse_partial,
                          OATTN_F32, stream);

@@ -255,3 +255,24 @@ def test_selftest_site_code_matches_binding():
     assert int(m.group(1), 16) == ops.SELFTEST_SITE
     src = open(os.path.join(ROOT, "online_softmax_gb300", "csrc", "selftest.cu")).read()
     assert re.search(r"kErrSelfTest\s*=\s*" + m.group(1), src)
+
+
+def noalloc(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A2, lse=None, B=1, H=1, Nq=1, Nkv=64, D=128, causal=0, scale=0.1, dt=1, P=4)
+    a.update(kw)
+    return lib.attn_fwd_splitk_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                                       a["Nkv"], a["D"], a["causal"], a["scale"], a["dt"], a["P"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Nq=0, dt=5), 1), (dict(Nq=0, scale=-1.0), 1), (dict(Nq=0, D=48), 2), (dict(Nq=0, dt=2), 2),
+    (dict(Nq=0, P=0), 1), (dict(Nq=0, P=257), 1), (dict(o=None), 1), (dict(Nq=0, Nkv=3, causal=1), 1),
+])
+def test_noalloc_checks_arguments_of_empty_problems_too(lib, kw, expect):
+    """The allocation-free split-K entry point refuses the same bad arguments as
+    attn_fwd_splitk, also when the problem is empty (Nq == 0)."""
+    assert noalloc(lib, **kw) == expect
+
+
+def test_noalloc_empty_problem_accepts_null_pointers(lib):
+    assert noalloc(lib, q=None, k=None, v=None, o=None, Nq=0) == 0

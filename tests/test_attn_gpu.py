@@ -117,20 +117,26 @@ def prefill_inputs(dtype="bf16"):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_full_size_sampled(causal):
-    B, Hh, N, D, seed = (PREFILL[x] for x in ("B", "H", "N", "D", "seed"))
+def test_prefill_full_size_every_row(causal):
+    """The whole prefill problem (B=4, H=32, N=4096, D=128, bf16) against the FP64 oracle:
+    every row of every head, in the launch configuration the bench times.  The inputs
+    are drawn on the device (bit-identical to the host generator, see
+    test_device_generator_bit_identical) and each head is copied back to the host for
+    the oracle, so a fault in how CTAs map to heads, query tiles or rows cannot hide
+    behind a sample."""
+    B, Hh, N, D = (PREFILL[x] for x in ("B", "H", "N", "D"))
     q, k, v = prefill_inputs()
     o, lse = run_attn(q, k, v, causal)
-    rng = np.random.default_rng(5)
-    rows = np.unique(np.r_[0, 1, 127, 128, 255, 256, 2047, 4095, rng.integers(0, N, 56)])
-    for bh in (0, 37, B * Hh - 1):
-        qr = H.head_slice(seed, synth.STREAM_Q, bh, N, D, "bf16", rows)
-        kh = H.head_slice(seed, synth.STREAM_K, bh, N, D, "bf16")
-        vh = H.head_slice(seed, synth.STREAM_V, bh, N, D, "bf16")
-        O_ref, L_ref = oracle.attention_rows(qr, rows, kh, vh, 1.0 / math.sqrt(D), causal)
+    scale = 1.0 / math.sqrt(D)
+    worst16, worst32 = 0.0, 0.0
+    for bh in range(B * Hh):
         b, h = divmod(bh, Hh)
-        H.check16(H.to_f64(o[b, h, rows]), O_ref, f"prefill bh{bh} O")
-        H.check32(H.to_f64(lse[b, h, rows]), L_ref, f"prefill bh{bh} LSE")
+        O_ref, L_ref = oracle.attention(H.to_f64(q[b, h]), H.to_f64(k[b, h]), H.to_f64(v[b, h]), scale, causal)
+        max_abs, _ = H.check16(H.to_f64(o[b, h]), O_ref, f"prefill b{b} h{h} O")
+        worst16 = max(worst16, max_abs)
+        worst32 = max(worst32, H.check32(H.to_f64(lse[b, h]), L_ref, f"prefill b{b} h{h} LSE"))
+    print(f"prefill causal={causal}: {B * Hh} heads x {N} rows, worst O max-abs {worst16:.2e}, "
+          f"worst LSE error {worst32:.2f} of the bound")
 
 
 def test_prefill_deterministic():

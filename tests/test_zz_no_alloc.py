@@ -1,17 +1,21 @@
-"""The allocation-free split-K entry point, checked against attn_fwd_splitk.
+"""The allocation-free split-K entry point, checked against the FP64 oracle and against
+attn_fwd_splitk.
 
 attn_fwd_splitk_noalloc serves callers that cannot allocate device memory: it keeps the
 partition workspace in a fixed array inside the library instead of caller buffers.
-These tests call it through the C ABI and compare it with the entry point that takes
-caller-owned workspace, on two calls in a row (the second call runs on a workspace
-that still holds the first call's partials).  The file sorts last so that a run that
-stops at the first failure has run every other test first."""
+These tests call it through the C ABI, on two calls in a row (the second call runs on a
+workspace that still holds the first call's partials), and compare each call with the
+FP64 oracle's attention (an independent check: a fault shared by both CUDA entry points
+would not hide) and with the entry point that takes caller-owned workspace.  The file
+sorts last so that a run that stops at the first failure has run every other test
+first."""
 import ctypes
 import math
 
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from tests import helpers as H
 
@@ -66,10 +70,14 @@ def test_noalloc_matches_caller_workspace(B, Hh, Nq, Nkv, D, P, causal):
     assert torch.cuda.is_available()
     qb, kb, vb = H.qkv_host(61, B, Hh, Nq, D, "bf16", nkv=Nkv)
     q, k, v = (H.to_device(x, "bf16") for x in (qb, kb, vb))
+    O_or, L_or = oracle.attention(synth.to_f64(qb, "bf16"), synth.to_f64(kb, "bf16"), synth.to_f64(vb, "bf16"),
+                                  1.0 / math.sqrt(D), causal)
     o_ref, lse_ref = _reference(ops, torch, q, k, v, P, causal)
     for call in range(2):
         o, lse = _noalloc(ops, torch, q, k, v, P, causal)
         torch.cuda.synchronize()
-        H.check16(H.to_f64(o), H.to_f64(o_ref), f"call {call} O")
-        H.check32(H.to_f64(lse), H.to_f64(lse_ref), f"call {call} LSE")
+        H.check16(H.to_f64(o), O_or, f"call {call} O vs oracle")
+        H.check32(H.to_f64(lse), L_or, f"call {call} LSE vs oracle")
+        H.check16(H.to_f64(o), H.to_f64(o_ref), f"call {call} O vs attn_fwd_splitk")
+        H.check32(H.to_f64(lse), H.to_f64(lse_ref), f"call {call} LSE vs attn_fwd_splitk")
     assert ops.device_error() == 0
