@@ -380,6 +380,97 @@ __device__ __forceinline__ int next_marked(const uint32_t* need, int from) {
   return w * 32 + __ffs(bits) - 1;
 }
 
+// One key tile of one query row (the calling thread's TMEM lane): read S, hide the keys
+// the optional mask hides (MASK; `w` = this row's 16 mask bytes for the tile), the keys
+// at or past kv_hi and, when causal, after the query; then p = 2^(s*scale*log2e - m),
+// the FP32 row sum into l, and P rounded to the input dtype written back over S.
+//
+// The stabiliser m only has to keep every p = 2^(x - m) finite and within the 16-bit P
+// operand's range; it need not be the row maximum.  So the maximum is taken only while
+// some row of the warp has seen no key, or when the tile's row sum of p exceeds kPBound
+// (p <= row sum): then the tile is redone against the exact maximum, O and l are
+// rescaled by alpha = 2^(m - m') (`rescale_ok`: O holds earlier tiles), and P is stored
+// again.  Exact arithmetic is unchanged; the common path has no maximum at all.
+template <class C, bool BF16, bool MASK>
+__device__ __forceinline__ void softmax_tile(uint32_t trow, uint32_t col_s, uint32_t col_o, bool rescale_ok,
+                                             int key0, int row, int row0, int kv_hi, int causal, float scale_log2,
+                                             uint4 w, float& m, float& l) {
+  constexpr int BN = C::BN_;
+  static_assert((BN - 8) % 16 == 8, "the row maximum walks 8 columns, then pairs of 8");
+  uint32_t u[BN];
+  tmem_load_cols<BN>(trow + col_s, u);
+  float s[BN];
+#pragma unroll
+  for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
+  if constexpr (MASK) {
+    const bool whole = (w.x & w.y & w.z & w.w) == ~0u;
+    if (!__all_sync(0xffffffffu, whole)) {  // a warp whose rows see the whole tile skips this
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) s[c] = ((ww[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+    }
+  }
+  if ((key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0)) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c) {
+      const int key = key0 + c;
+      s[c] = (key < kv_hi && (!causal || key <= row)) ? s[c] : -INFINITY;
+    }
+  }
+  bool exact = !__all_sync(0xffffffffu, m != -INFINITY);
+  float rowsum;
+  for (;;) {
+    if (exact) {
+      // row max: 8 independent chains of three-input max
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c + 16 <= BN; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[BN - 8 + i]);
+      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+      const float mnew = fmaxf(m, mx * scale_log2);
+      const float alpha = (mnew == m) ? 1.f : ex2(m - mnew);  // ex2(-inf) = 0
+      if (rescale_ok && __any_sync(0xffffffffu, alpha != 1.f)) tmem_scale_cols<C::D_>(trow + col_o, alpha);
+      l *= alpha;
+      m = mnew;
+    }
+    const float nbase = (m == -INFINITY) ? 0.f : -m;
+    // p per chunk of CW columns: the scale-and-shift on pairs (f32x2 FMA), then all CW
+    // exponentials on the MUFU (independent, so their latencies overlap), then the row
+    // sum on pairs (f32x2 add, four chains) and the 16-bit packing.  Chunks of 64
+    // columns measured ~1% faster than chunks of 32 or 16.
+    constexpr int CW = BN < 64 ? BN : 64;
+    float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c2 = 0; c2 < BN / CW; ++c2) {
+      uint32_t pk[CW / 2];
+      float xx[CW];
+#pragma unroll
+      for (int i = 0; i < CW / 2; ++i)
+        ffma2(xx[2 * i], xx[2 * i + 1], s[c2 * CW + 2 * i], s[c2 * CW + 2 * i + 1], scale_log2, scale_log2, nbase,
+              nbase);
+#pragma unroll
+      for (int i = 0; i < CW; ++i) xx[i] = ex2(xx[i]);
+#pragma unroll
+      for (int i = 0; i < CW / 2; ++i) {
+        fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], xx[2 * i], xx[2 * i + 1]);
+        pk[i] = pack2<BF16>(xx[2 * i], xx[2 * i + 1]);
+      }
+      if constexpr (CW == 64) tmem_st_x32(trow + col_s + c2 * 32, pk);
+      else tmem_st_x16(trow + col_s + c2 * 16, pk);
+    }
+    tmem_wait_st();
+    rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+    if (exact || __all_sync(0xffffffffu, rowsum <= kPBound)) break;  // NaN/inf fail the test
+    exact = true;
+  }
+  l += rowsum;
+}
+
 __device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -677,85 +768,8 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        uint32_t u[BN];
-        tmem_load_cols<BN>(trow + col_s, u);
-        float s[BN];
-#pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
-
-        if constexpr (MASK) {
-          const bool whole = (w.x & w.y & w.z & w.w) == ~0u;
-          if (!__all_sync(0xffffffffu, whole)) {
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int c = 0; c < BN; ++c) s[c] = ((ww[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
-          }
-        }
-        const int key0 = kv_lo + tj * BN;
-        if ((key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0)) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int key = key0 + c;
-            const bool vis = key < kv_hi && (!causal || key <= row);
-            s[c] = vis ? s[c] : -INFINITY;
-          }
-        }
-        // The stabiliser m only has to keep every p = 2^(x - m) finite and within the
-        // 16-bit P operand's range; it need not be the row maximum.  So the maximum is
-        // taken only when some row of the warp has seen no key yet, or when this tile's
-        // exponentials exceed kPBound (p <= row sum): then the tile is redone against the
-        // exact new maximum, O and l are rescaled by alpha = 2^(m - m'), and P is stored
-        // again.  Exact arithmetic is unchanged; the common path has no max at all.
-        bool exact = !__all_sync(0xffffffffu, m != -INFINITY);
-        float rowsum;
-        for (;;) {
-          if (exact) {
-            // row max: 8 independent chains of three-input max
-            float m8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) m8[i] = s[i];
-#pragma unroll
-            for (int c = 8; c < BN; c += 16)
-#pragma unroll
-              for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
-            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            const float mnew = fmaxf(m, mx * scale_log2);
-            const float alpha = (mnew == m) ? 1.f : ex2(m - mnew);  // ex2(-inf) = 0
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) tmem_scale_cols<D>(trow + col_o, alpha);
-            l *= alpha;
-            m = mnew;
-          }
-          const float nbase = (m == -INFINITY) ? 0.f : -m;
-          // p = 2^(s*scale*log2e - m) per chunk of CW columns: the scale-and-shift runs on
-          // pairs (f32x2 FMA), then all CW exponentials on the MUFU (independent, so their
-          // latencies overlap), then the row sum on pairs (f32x2 add, four chains) and the
-          // 16-bit packing.  Chunks of 64 columns measured ~1% faster than chunks of 32 or
-          // 16 (more independent work between the dependent stages).
-          constexpr int CW = BN < 64 ? BN : 64;
-          float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int c2 = 0; c2 < BN / CW; ++c2) {
-            uint32_t pk[CW / 2];
-            float xx[CW];
-#pragma unroll
-            for (int i = 0; i < CW / 2; ++i)
-              ffma2(xx[2 * i], xx[2 * i + 1], s[c2 * CW + 2 * i], s[c2 * CW + 2 * i + 1], scale_log2, scale_log2, nbase, nbase);
-#pragma unroll
-            for (int i = 0; i < CW; ++i) xx[i] = ex2(xx[i]);
-#pragma unroll
-            for (int i = 0; i < CW / 2; ++i) {
-              fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], xx[2 * i], xx[2 * i + 1]);
-              pk[i] = pack2<BF16>(xx[2 * i], xx[2 * i + 1]);
-            }
-            if constexpr (CW == 64) tmem_st_x32(trow + col_s + c2 * 32, pk);
-            else tmem_st_x16(trow + col_s + c2 * 16, pk);
-          }
-          tmem_wait_st();
-          rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-          if (exact || __all_sync(0xffffffffu, rowsum <= kPBound)) break;  // NaN/inf fail the test
-          exact = true;
-        }
-        l += rowsum;
+        softmax_tile<C, BF16, MASK>(trow, col_s, col_o, j > 0, kv_lo + tj * BN, row, row0, kv_hi, causal, scale_log2, w,
+                                    m, l);
         tc_fence_before();
         mbar_arrive(&bar_p[t]);
       }
