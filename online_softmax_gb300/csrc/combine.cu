@@ -8,12 +8,15 @@
 // five for the sum); each partition's scale is then broadcast from its owning lane
 // with one indexed shuffle, and the depth vector of the next partition step is loaded
 // (128-bit loads) before the current one is folded in; the first steps are requested
-// before the LSE reduction, whose loads they do not depend on.  When a partition row is
-// shorter than a warp of 128-bit vectors (16-bit data, depth 128), the warp splits into
-// 32/LPP groups that take consecutive partitions and are summed at the end.  Ladder
-// sizes P in {2, 4, 8, 16, 32} get fully unrolled instances (P <= 4 with eight or
-// four row-heads per warp, all their loads in flight at once); any other P runs the
-// runtime-bound loop, streaming four steps ahead.
+// before the LSE reduction, whose loads they do not depend on.  Ladder sizes P in
+// {2, 4, 8, 16, 32} get fully unrolled instances; any other P runs a runtime-bound loop.
+// Rows shorter than a warp of 128-bit vectors:
+//   * at P = 2 and 4 every lane owns one vector of a row-head and folds all partitions
+//     itself, several row-heads per warp with all loads in flight;
+//   * rows of 16 vectors (16-bit data at depth 128), any other P: half a warp owns a
+//     row-head end to end (two per warp), so nothing is summed across half-warps;
+//   * other short rows: the warp splits into 32/LPP groups that take consecutive
+//     partitions of one row-head and are summed at the end.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -417,6 +420,125 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   }
 }
 
+// Rows shorter than a warp of 16-byte vectors (LPP < 32 lanes per row, e.g. 16-bit data
+// at depth 128): each group of LPP lanes owns one row-head end to end, 32/LPP row-heads
+// per warp.  The LSE reduction and the scale broadcasts stay inside the group
+// (width-LPP shuffles), every lane folds all P partitions of its 16-byte vector, and
+// nothing is summed across groups at the end.  AHEAD partition vectors per lane are in
+// flight while the current one is folded.
+template <typename TIn, typename TOut, int LPP, int P_STATIC>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    splitk_combine_group_kernel(const TIn* __restrict__ o_partial, const float* __restrict__ lse_partial,
+                                TOut* __restrict__ out, float* __restrict__ lse_out, int P_rt, long long RH,
+                                float lse_scale) {
+  constexpr int E = Vec<TIn>::E;
+  constexpr int G = 32 / LPP;  // row-heads per warp
+  constexpr int DEPTH = LPP * E;
+  constexpr int SLOTS = P_STATIC > 0 ? (P_STATIC + LPP - 1) / LPP : kMaxP / LPP;
+  constexpr int AHEAD = 8;
+  static_assert(LPP < 32 && 32 % LPP == 0, "a row-head takes a whole number of lanes");
+  static_assert(P_STATIC > 0 || G * kMaxP * kCombineWarps * 4 <= 32768, "runtime-P scales fit shared memory");
+  const int P = P_STATIC > 0 ? P_STATIC : P_rt;
+
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const long long rh0 = ((long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5)) * G;
+  if (rh0 >= RH) return;  // whole warp leaves together
+  const int g = lane / LPP, li = lane % LPP;
+  const long long rh = rh0 + g;
+  const bool valid = rh < RH;
+  const TIn* base = o_partial + rh * DEPTH + li * E;
+  const long long pstride = RH * (long long)DEPTH;
+  auto load = [&](int p) {
+    return (valid && p < P) ? __ldcs(reinterpret_cast<const uint4*>(base + p * pstride)) : make_uint4(0u, 0u, 0u, 0u);
+  };
+
+  // The first partition vectors are requested before the LSE reduction.
+  uint4 x[AHEAD];
+#pragma unroll
+  for (int i = 0; i < AHEAD; ++i) x[i] = load(i);
+
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  auto fold = [&](float sc, const uint4 v) {
+    float w[E];
+    widen_vec<TIn>(v, w);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(sc, (sc != 0.f) ? w[e] : 0.f, acc[e]);
+  };
+  bool dead;
+  float Gl;
+  if constexpr (P_STATIC > 0) {
+    // ---- LSE reduction inside the group: lane li keeps partitions li, li + LPP, ...
+    float lse[SLOTS];
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int p = s * LPP + li;
+      lse[s] = (valid && p < P) ? __ldg(lse_partial + (long long)p * RH + rh) : -INFINITY;
+      m = fmaxf(m, lse[s]);
+    }
+#pragma unroll
+    for (int o = LPP / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    dead = (m == -INFINITY);
+    const float msafe = dead ? 0.f : m;
+    float sum = 0.f;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) sum += ex2(lse[s] - msafe);  // ex2(-inf) = +0
+#pragma unroll
+    for (int o = LPP / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    Gl = dead ? -INFINITY : lg2(sum) + msafe;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) lse[s] = dead ? 0.f : ex2(lse[s] - Gl);  // now scale_p
+#pragma unroll
+    for (int p = 0; p < P_STATIC; ++p) {
+      const float sc = __shfl_sync(0xffffffffu, lse[p / LPP], p % LPP, LPP);
+      const uint4 cur = x[p % AHEAD];
+      if (p + AHEAD < P_STATIC) x[p % AHEAD] = load(p + AHEAD);
+      fold(sc, cur);
+    }
+  } else {
+    // Runtime P: the group's LSEs, then its scales, live in its own shared-memory row
+    // (a run-time register index would spill), so no per-lane arrays are kept; the
+    // vectors stream through one rolling buffer of AHEAD.
+    __shared__ float s_scale[kCombineWarps][G][kMaxP];
+    float* my = s_scale[threadIdx.x >> 5][g];
+    float m = -INFINITY;
+    for (int p = li; p < P; p += LPP) {
+      const float v = valid ? __ldg(lse_partial + (long long)p * RH + rh) : -INFINITY;
+      my[p] = v;
+      m = fmaxf(m, v);
+    }
+#pragma unroll
+    for (int o = LPP / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    dead = (m == -INFINITY);
+    const float msafe = dead ? 0.f : m;
+    float sum = 0.f;
+    for (int p = li; p < P; p += LPP) sum += ex2(my[p] - msafe);
+#pragma unroll
+    for (int o = LPP / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    Gl = dead ? -INFINITY : lg2(sum) + msafe;
+    for (int p = li; p < P; p += LPP) my[p] = dead ? 0.f : ex2(my[p] - Gl);
+    __syncwarp();
+    for (int p0 = 0; p0 < P; p0 += AHEAD) {
+#pragma unroll
+      for (int i = 0; i < AHEAD; ++i) {
+        const uint4 cur = x[i];
+        x[i] = load(p0 + AHEAD + i);
+        if (p0 + i < P) fold(my[p0 + i], cur);
+      }
+    }
+  }
+  if (valid) {
+    float y[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) y[e] = dead ? 0.f : acc[e] + 0.f;
+    store_vec<TOut, E>(out + rh * DEPTH + li * E, y);
+    if (lse_out != nullptr && li == 0) lse_out[rh] = dead ? -INFINITY : Gl * lse_scale;
+  }
+}
+
 template <typename TIn, typename TOut, int LPP, int VPL>
 cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P, long long RH,
                      float lse_scale, bool pdl, cudaStream_t st) {
@@ -442,6 +564,17 @@ cudaError_t launch_p(const void* op, const float* lp, void* o, float* lo, int P,
                    : launch_maybe_pdl(pdl, splitk_combine_lane_kernel<TIn, TOut, LPP, 4, 2>, grid_lane4, block, st, a, lp, c, lo, RH, lse_scale);
       return e != cudaSuccess ? e : cudaGetLastError();
     }
+  }
+  if constexpr (LPP == 16 && VPL == 1) {
+    // Rows of 16 vectors (16-bit data at depth 128), any other P: half a warp per row-head.
+    const dim3 grid_group((unsigned)((RH + kCombineWarps * kLaneG - 1) / (kCombineWarps * kLaneG)));
+    switch (P) {
+      case 8: e = launch_maybe_pdl(pdl, splitk_combine_group_kernel<TIn, TOut, LPP, 8>, grid_group, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+      case 16: e = launch_maybe_pdl(pdl, splitk_combine_group_kernel<TIn, TOut, LPP, 16>, grid_group, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+      case 32: e = launch_maybe_pdl(pdl, splitk_combine_group_kernel<TIn, TOut, LPP, 32>, grid_group, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+      default: e = launch_maybe_pdl(pdl, splitk_combine_group_kernel<TIn, TOut, LPP, 0>, grid_group, block, st, a, lp, c, lo, P, RH, lse_scale); break;
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
   switch (P) {
     case 2: e = launch_maybe_pdl(pdl, splitk_combine_small_kernel<TIn, TOut, LPP, VPL, 2, R2>, grid_small2, block, st, a, lp, c, lo, RH, lse_scale); break;
