@@ -738,6 +738,7 @@ def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps, cpu=False):
         heavy.append({"P": P, "us_pdl": med * 1e6, "us_separate_calls": med_sep * 1e6, "pdl_speedup": med_sep / med})
     out["pdl_combine_heavy"] = {"workload": "1 sequence x 1 query, 32 heads, 32768 keys, D=128, bf16, P in {37, 148}",
                                 "results": heavy}
+    out["multi_query"] = measure_splitk_prefill(torch, ops, sc, synth, dev)
     assert ops.device_error() == 0
     fr = [r["frac"] for r in out["results"]]
     fd = [r["frac_datasheet"] for r in out["results"]]
@@ -748,6 +749,35 @@ def measure_decode(torch, ops, sc, synth, pk, dev, Bd, Ps, cpu=False):
     if cpu:
         out["cpu_baseline"] = decode_cpu_baseline(6.0, Ps)
     return out
+
+
+def measure_splitk_prefill(torch, ops, sc, synth, dev):
+    """Split-K over query tiles (the tensor-core split path): B=1, H=32, N=4096, D=128,
+    bf16, causal, P = 4 and 8.  The PDL-launched combine of attn_fwd_splitk against the
+    same two kernels as separate calls and against the in-kernel merge."""
+    Bq, Hq, Nq, Dq = 1, 32, 4096, 128
+    mk = lambda sid: sc.fill_normal(torch.empty((Bq, Hq, Nq, Dq), dtype=torch.bfloat16, device=dev), 7, sid, "bf16")
+    q, k, v = mk(synth.STREAM_Q), mk(synth.STREAM_K), mk(synth.STREAM_V)
+    o = torch.empty_like(q)
+    res = []
+    for P in (4, 8):
+        op = torch.empty((P, Bq * Hq * Nq, Dq), dtype=torch.float32, device=dev)
+        lp = torch.empty((P, Bq * Hq * Nq), dtype=torch.float32, device=dev)
+        counters = torch.zeros(ops.attn_splitk_counters(Bq, Hq, Nq), dtype=torch.int32, device=dev)
+        fn = lambda: ops.attn_fwd_splitk(q, k, v, P, op, lp, o, None, causal=True)
+        fn_sep = lambda: (ops.attn_fwd_splitk(q, k, v, P, op, lp, None, None, causal=True),
+                          ops.splitk_combine(op, lp, o.view(-1, Dq), rows=Nq, heads=Hq))
+        fn_fused = lambda: ops.attn_fwd_splitk_fused(q, k, v, P, op, lp, counters, o, None, causal=True)
+        for f in (fn, fn_sep, fn_fused):
+            for _ in range(3):
+                f()
+        med = time_launches(torch, fn, 20)[0]
+        med_sep = time_launches(torch, fn_sep, 20)[0]
+        med_fused = time_launches(torch, fn_fused, 20)[0]
+        res.append({"P": P, "us_pdl": med * 1e6, "us_separate_calls": med_sep * 1e6, "us_fused_merge": med_fused * 1e6,
+                    "pdl_speedup": med_sep / med, "fused_speedup": med / med_fused})
+    assert ops.device_error() == 0
+    return {"workload": "split-K over query tiles: B=1, H=32, N=4096, D=128, bf16, causal", "results": res}
 
 
 def decode_cpu_baseline(budget_s: float, Ps):
