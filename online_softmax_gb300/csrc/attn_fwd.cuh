@@ -72,6 +72,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -597,8 +598,9 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* abort = &s_abort;
 
   // Masked instances: the softmax warps mark every key tile that some row of theirs
-  // sees (lane = key tile, one coalesced 512-byte load per row and 32 tiles; the rows a
-  // causal tile cannot reach are not looked at), then every role counts and walks the
+  // sees (lane = key tile, one coalesced 512-byte load per row and 32 tiles, 8 rows at a
+  // time until the lane has seen a visible key; the key tiles a causal query tile cannot
+  // reach are not looked at), then every role counts and walks the
   // marked tiles only (tile 0 is always marked: it is already on its way).  A skipped
   // tile has no visible key for any row of the CTA, so leaving it out changes no result.
   int nkv0 = nkv0_all, nkv1 = nkv1_all;
@@ -613,17 +615,23 @@ __global__ void __launch_bounds__(384, 1)
         for (int g = 0; g * 32 < n_t; ++g) {
           const int j = g * 32 + lane;
           uint32_t acc = 0u;
-#pragma unroll 1
-          for (int r0 = 0; r0 < 32; r0 += 16) {
-            uint4 w[16];
+          // The first 8 rows, then the other 24 only for lanes that have not yet seen a
+          // visible key: a tile that is needed usually shows it at once, and only tiles
+          // that end up skipped are read for all 32 rows (in two rounds).
+          auto scan_rows = [&](auto nrows_c, int r0) {
+            constexpr int NR = decltype(nrows_c)::value;
+            uint4 w[NR];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < NR; ++i) {
               const int row = rbase + r0 + i;
-              w[i] = (j < n_t && row < N) ? ld_mask16(base + (long long)row * mk.sq + 4 * j) : make_uint4(0u, 0u, 0u, 0u);
+              w[i] = row < N ? ld_mask16(base + (long long)row * mk.sq + 4 * j) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc |= w[i].x | w[i].y | w[i].z | w[i].w;
-          }
+            for (int i = 0; i < NR; ++i) acc |= w[i].x | w[i].y | w[i].z | w[i].w;
+          };
+          if (j < n_t) scan_rows(std::integral_constant<int, 8>{}, 0);
+          if (__any_sync(0xffffffffu, j < n_t && acc == 0u) && j < n_t && acc == 0u)
+            scan_rows(std::integral_constant<int, 24>{}, 8);
           const uint32_t marks = __ballot_sync(0xffffffffu, acc != 0u);
           if (lane == 0 && marks != 0u) atomicOr(&s_need[g], marks);
         }
