@@ -88,10 +88,11 @@ def test_combine_full_size(P, dtype):
     assert torch.all(torch.isneginf(g[torch.from_numpy(dead).cuda()]))
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 64, 100, 256])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16, 32, 64, 100, 256])
 @pytest.mark.parametrize("depth,in_dt,out_dt", [(128, "f32", "f32"), (64, "bf16", "bf16"),
                                                 (256, "f16", "f32"), (32, "f32", "bf16"),
-                                                (16, "bf16", "f16"), (128, "bf16", "f32")])
+                                                (16, "bf16", "f16"), (128, "bf16", "f32"),
+                                                (128, "f16", "f16"), (64, "f32", "f32")])
 def test_combine_small_full_oracle(P, depth, in_dt, out_dt):
     seed, RH = 30 + P, 300
     o_b = synth.tensor(seed, synth.STREAM_OPART, (P, RH, depth), in_dt)
