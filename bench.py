@@ -426,7 +426,9 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
                      "peak_source": f"{pk_kind} (dense bf16 burst)", "kernel": "attn_fwd_kernel<128,128,bf16>",
-                     **clock_aware_roofline(torch, dev, achieved, pk, clocks)},
+                     **clock_aware_roofline(achieved, pk, clocks,
+                                             torch.cuda.get_device_properties(dev).multi_processor_count,
+                                             peak_run_mhz())},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
@@ -454,7 +456,16 @@ def pci_bus_id(torch, dev):
 FLOP_PER_SM_CLOCK = 2 * 128 * 128 * 16 / 64
 
 
-def clock_aware_roofline(torch, dev, achieved, pk, clocks):
+def peak_run_mhz():
+    """Median SM clock under load recorded beside the measured peaks (None if absent)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["clocks_under_load"]["sm_mhz_median"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+def clock_aware_roofline(achieved, pk, clocks, sms, peak_mhz):
     """The attention rate against peaks that account for the SM clock.  The measured
     cuBLAS peak was taken at the power-capped clock recorded beside it (median under
     load), while this kernel runs at the clock sampled during its timed region:
@@ -462,13 +473,7 @@ def clock_aware_roofline(torch, dev, achieved, pk, clocks):
       frac_of_clock_peak = achieved / (SMs * FLOP_PER_SM_CLOCK * kernel's MHz)."""
     out = {}
     mhz = clocks.get("sm_mhz")
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak_mhz = float(json.load(f)["clocks_under_load"]["sm_mhz_median"])
-    except (OSError, KeyError, ValueError, TypeError):
-        peak_mhz = None
     if mhz:
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         at_clock = sms * FLOP_PER_SM_CLOCK * mhz * 1e6 / 1e12
         out["kernel_sm_mhz"] = mhz
         out["peak_at_kernel_clock"] = at_clock

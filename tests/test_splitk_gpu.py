@@ -212,3 +212,24 @@ def test_splitk_max_partitions(Nq):
         O, L = oracle.attention_rows(qr, rows, kh, vh, 1.0 / math.sqrt(D), False)
         H.check16(H.to_f64(o[0, bh, rows]), O, f"P256 Nq{Nq} bh{bh} O")
         H.check32(H.to_f64(lse[0, bh, rows]), L, f"P256 Nq{Nq} bh{bh} LSE")
+
+
+@pytest.mark.parametrize("RH", [1, 3, 301, 1027])
+@pytest.mark.parametrize("P", [2, 3, 8, 16, 37])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_combine_16bit_rows_ragged_row_heads(RH, P, dtype):
+    """16-bit partials at depth 128 (the half-warp-per-row-head kernels, several row-heads
+    per half-warp at P = 8) with row-head counts that leave a warp partly empty."""
+    seed, depth = 400 + RH + P, 128
+    o_b = synth.tensor(seed, synth.STREAM_OPART, (P, RH, depth), dtype)
+    lse = synth.lse_partials(seed, P, RH, drop=0.2, row_drop=0.05)
+    op = H.to_device(o_b, dtype)
+    lp = torch.from_numpy(lse).cuda()
+    o = torch.full((RH + 1, depth), 7.0, dtype=H.torch_dtype(dtype), device="cuda")  # one guard row
+    g = torch.full((RH + 1,), 7.0, dtype=torch.float32, device="cuda")
+    ops.splitk_combine(op, lp, o[:RH], g[:RH])
+    torch.cuda.synchronize()
+    O_ref, G_ref = oracle.combine(synth.to_f64(o_b, dtype), lse)
+    H.check16(H.to_f64(o[:RH]), O_ref, f"RH{RH} P{P} O")
+    H.check32(H.to_f64(g[:RH]), G_ref, f"RH{RH} P{P} G")
+    assert torch.all(o[RH] == 7.0) and g[RH].item() == 7.0, "a row-head past the end was written"
