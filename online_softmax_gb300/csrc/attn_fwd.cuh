@@ -16,8 +16,9 @@
 //   * A CTA owns two 128-row query tiles of one head (and one split-K partition in
 //     split mode).  Warps 0-3 and 4-7 are two softmax warpgroups, one per query tile;
 //     thread r of a warpgroup owns row r, which is TMEM lane r, so row max and row sum
-//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs, warp 10
-//     watches the K/V copies for the MMA issuer (see below); warps 10-11 also complete
+//     need no shuffles.  Warp 8 issues TMA copies, warp 9 issues the MMAs (all its
+//     lanes walk the issue loop, one elected lane issues), warp 10 watches the K/V
+//     copies for the MMA issuer (see below); warps 10-11 also complete
 //     the third warpgroup so that setmaxnreg can move its registers to the softmax
 //     warpgroups (216 per softmax thread).
 //   * Q tiles are copied once; K and V tiles stream through a ring of shared-memory
@@ -26,13 +27,15 @@
 //     Keys past the end of the sequence arrive as zeros (out-of-bounds fill).
 //   * S_t = Q_t K^T is a kind::f16 MMA (M=128, N=BN, K=D) into TMEM columns
 //     [t*BN, (t+1)*BN).  The softmax threads read their row (tcgen05.ld), mask with
-//     -inf, compute p = 2^(s*scale*log2e - m) with one FMA and one ex2.approx each (in
-//     chunks of 64 columns), sum the FP32 p, round p to the input dtype (cvt.rn, round
-//     to nearest even) and write it back over S (tcgen05.st) as the A operand of
+//     -inf, compute p = 2^(s*scale*log2e - m) with one FMA and one ex2.approx each,
+//     sum the FP32 p, round p to the input dtype (cvt.rn, round to nearest even) and
+//     write it back over S (tcgen05.st) as the A operand of
 //     O_t += P V (M=128, N=D, K=BN, A from TMEM, B = V tile read MN-major).
-//   * The single MMA-issuing thread is the critical path: each mbarrier wait it makes
-//     costs it ~150-200 cycles while the tensor pipe streams shared memory, even when
-//     the phase has already completed.  So it waits once per group: bar_p[t] counts the
+//   * The MMA issuer is the critical path: one MMA of M=128, N=128, K=16 takes the
+//     tensor pipe 64 cycles, about as long as issuing it takes.  The issue loop runs on
+//     all 32 lanes of warp 9 with the issuing lane picked once by elect.sync, so every
+//     descriptor and address is warp-uniform (a lone-thread loop measured 5% slower).
+//     The issuer waits once per group: bar_p[t] counts the
 //     128 softmax threads of tile t AND a watcher thread that has seen V_j and K_(j+1)
 //     land, so one completed phase means "P_t(j) written, PV_t(j) and S_t(j+1) may
 //     start".  The watcher never arrives for phase j before phase j - 1 completed.
@@ -213,7 +216,7 @@ __device__ __forceinline__ bool wait_kv(uint64_t* full, int n, int& ready, volat
 // leading byte offset >> 4) and a high word (stride byte offset >> 4, the fixed 0b001 and
 // the swizzle mode) that is the same for every operand here.  Consecutive K steps only
 // move the start address, so each MMA costs one 32-bit add on a precomputed low word:
-// the single issuing thread must keep up with 64-cycle MMAs.
+// the issuer must keep up with 64-cycle MMAs.
 template <class C>
 __device__ __forceinline__ uint32_t desc_hi() {
   return (uint32_t)(((8 * C::SW) >> 4) & 0x3FFF) | (1u << 14) | (C::SWZ << 29);
@@ -387,20 +390,22 @@ __device__ __forceinline__ int next_marked(const uint32_t* need, int from) {
 // the FP32 row sum into l, and P rounded to the input dtype written back over S.
 //
 // The stabiliser m only has to keep every p = 2^(x - m) finite and within the 16-bit P
-// operand's range; it need not be the row maximum.  So the maximum is taken only while
-// some row of the warp has seen no key, or when the tile's row sum of p exceeds kPBound
-// (p <= row sum): then the tile is redone against the exact maximum, O and l are
-// rescaled by alpha = 2^(m - m') (`rescale_ok`: O holds earlier tiles), and P is stored
-// again.  Exact arithmetic is unchanged; the common path has no maximum at all.
-template <class C, bool BF16, bool MASK>
-__device__ __forceinline__ void softmax_tile(uint32_t trow, uint32_t col_s, uint32_t col_o, bool rescale_ok,
-                                             int key0, int row, int row0, int kv_hi, int causal, float scale_log2,
-                                             uint4 w, float& m, float& l) {
+// operand's range; it need not be the row maximum.  So the common path takes no row
+// maximum: it computes p against the current m in registers and accepts the tile when
+// every row sum of p in the warp is at most kPBound (p <= row sum).  Otherwise, and
+// while some row of the warp has seen no key, the tile is done against the exact
+// maximum: the scores are read again from TMEM (P is only stored once the tile is
+// accepted, so S is still there), O and l are rescaled by alpha = 2^(m - m')
+// (`rescale_ok`: O holds earlier tiles) and p is computed again.  Exact arithmetic is
+// unchanged.  Not keeping the raw scores for that rare second pass leaves the
+// registers free for the scale, exponential, sum and packing stages of all columns to
+// overlap.
+template <class C, bool MASK>
+__device__ __forceinline__ void load_scores(uint32_t taddr, int key0, int row, int row0, int kv_hi, int causal,
+                                            uint4 w, float (&s)[C::BN_]) {
   constexpr int BN = C::BN_;
-  static_assert((BN - 8) % 16 == 8, "the row maximum walks 8 columns, then pairs of 8");
   uint32_t u[BN];
-  tmem_load_cols<BN>(trow + col_s, u);
-  float s[BN];
+  tmem_load_cols<BN>(taddr, u);
 #pragma unroll
   for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
   if constexpr (MASK) {
@@ -412,64 +417,89 @@ __device__ __forceinline__ void softmax_tile(uint32_t trow, uint32_t col_s, uint
     }
   }
   if ((key0 + BN > kv_hi) || (causal && key0 + BN - 1 > row0)) {
+    // key key0 + c is used when it is below kv_hi and, causal, at most the query row
+    const int lim = (causal ? min(kv_hi, row + 1) : kv_hi) - key0;
 #pragma unroll
-    for (int c = 0; c < BN; ++c) {
-      const int key = key0 + c;
-      s[c] = (key < kv_hi && (!causal || key <= row)) ? s[c] : -INFINITY;
+    for (int c = 0; c < BN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+  }
+}
+
+// p = 2^(s*scale_log2 + nbase) for a whole tile, in place: the scale-and-shift on pairs
+// (f32x2 FMA), the exponentials on the MUFU, the FP32 row sum on pairs (f32x2 add, four
+// chains) and the 16-bit packing (RNE) into pk.  All columns are independent, so the
+// stages of different columns overlap.
+template <int BN, bool BF16>
+__device__ __forceinline__ float exp_pack(float (&s)[BN], float scale_log2, float nbase, uint32_t (&pk)[BN / 2]) {
+#pragma unroll
+  for (int i = 0; i < BN / 2; ++i)
+    ffma2(s[2 * i], s[2 * i + 1], s[2 * i], s[2 * i + 1], scale_log2, scale_log2, nbase, nbase);
+#pragma unroll
+  for (int i = 0; i < BN; ++i) s[i] = ex2(s[i]);
+  float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < BN / 2; ++i) {
+    fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], s[2 * i], s[2 * i + 1]);
+    pk[i] = pack2<BF16>(s[2 * i], s[2 * i + 1]);
+  }
+  return ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+}
+
+template <int BN>
+__device__ __forceinline__ void store_p(uint32_t taddr, const uint32_t (&pk)[BN / 2]) {
+  if constexpr (BN / 2 >= 32) {
+#pragma unroll
+    for (int c = 0; c < BN / 64; ++c)
+      tmem_st_x32(taddr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
+  } else {
+    tmem_st_x16(taddr, pk);
+  }
+  tmem_wait_st();
+}
+
+
+template <class C, bool BF16, bool MASK>
+__device__ __forceinline__ void softmax_tile(uint32_t trow, uint32_t col_s, uint32_t col_o, bool rescale_ok,
+                                             int key0, int row, int row0, int kv_hi, int causal, float scale_log2,
+                                             uint4 w, float& m, float& l) {
+  constexpr int BN = C::BN_;
+  static_assert((BN - 8) % 16 == 8, "the row maximum walks 8 columns, then pairs of 8");
+  if (__all_sync(0xffffffffu, m != -INFINITY)) {
+    float s[BN];
+    uint32_t pk[BN / 2];
+    load_scores<C, MASK>(trow + col_s, key0, row, row0, kv_hi, causal, w, s);
+    const float rowsum = exp_pack<BN, BF16>(s, scale_log2, -m, pk);
+    if (__all_sync(0xffffffffu, rowsum <= kPBound)) {  // NaN/inf fail the test
+      store_p<BN>(trow + col_s, pk);
+      l += rowsum;
+      return;
     }
   }
-  bool exact = !__all_sync(0xffffffffu, m != -INFINITY);
-  float rowsum;
-  for (;;) {
-    if (exact) {
-      // row max: 8 independent chains of three-input max
-      float m8[8];
+  float s[BN];
+  uint32_t pk[BN / 2];
+  load_scores<C, MASK>(trow + col_s, key0, row, row0, kv_hi, causal, w, s);
+  // row max: 8 independent chains of three-input max
+  float m8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = s[i];
+  for (int i = 0; i < 8; ++i) m8[i] = s[i];
 #pragma unroll
-      for (int c = 8; c + 16 <= BN; c += 16)
+  for (int c = 8; c + 16 <= BN; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[BN - 8 + i]);
-      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-      const float mnew = fmaxf(m, mx * scale_log2);
-      const float alpha = (mnew == m) ? 1.f : ex2(m - mnew);  // ex2(-inf) = 0
-      if (rescale_ok && __any_sync(0xffffffffu, alpha != 1.f)) tmem_scale_cols<C::D_>(trow + col_o, alpha);
-      l *= alpha;
-      m = mnew;
-    }
-    const float nbase = (m == -INFINITY) ? 0.f : -m;
-    // p per chunk of CW columns: the scale-and-shift on pairs (f32x2 FMA), then all CW
-    // exponentials on the MUFU (independent, so their latencies overlap), then the row
-    // sum on pairs (f32x2 add, four chains) and the 16-bit packing.  Chunks of 64
-    // columns measured ~1% faster than chunks of 32 or 16.
-    constexpr int CW = BN < 64 ? BN : 64;
-    float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int c2 = 0; c2 < BN / CW; ++c2) {
-      uint32_t pk[CW / 2];
-      float xx[CW];
-#pragma unroll
-      for (int i = 0; i < CW / 2; ++i)
-        ffma2(xx[2 * i], xx[2 * i + 1], s[c2 * CW + 2 * i], s[c2 * CW + 2 * i + 1], scale_log2, scale_log2, nbase,
-              nbase);
-#pragma unroll
-      for (int i = 0; i < CW; ++i) xx[i] = ex2(xx[i]);
-#pragma unroll
-      for (int i = 0; i < CW / 2; ++i) {
-        fadd2(sum8[2 * (i & 3)], sum8[2 * (i & 3) + 1], xx[2 * i], xx[2 * i + 1]);
-        pk[i] = pack2<BF16>(xx[2 * i], xx[2 * i + 1]);
-      }
-      if constexpr (CW == 64) tmem_st_x32(trow + col_s + c2 * 32, pk);
-      else tmem_st_x16(trow + col_s + c2 * 16, pk);
-    }
+  for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[BN - 8 + i]);
+  const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+  const float mnew = fmaxf(m, mx * scale_log2);
+  const float alpha = (mnew == m) ? 1.f : ex2(m - mnew);  // ex2(-inf) = 0
+  m = mnew;
+  const float rowsum = exp_pack<BN, BF16>(s, scale_log2, (m == -INFINITY) ? 0.f : -m, pk);
+  store_p<BN>(trow + col_s, pk);
+  // O is rescaled last, when the scores and P no longer occupy registers (PV of this
+  // tile starts only after the arrival that follows)
+  if (rescale_ok && __any_sync(0xffffffffu, alpha != 1.f)) {
+    tmem_scale_cols<C::D_>(trow + col_o, alpha);
     tmem_wait_st();
-    rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-    if (exact || __all_sync(0xffffffffu, rowsum <= kPBound)) break;  // NaN/inf fail the test
-    exact = true;
   }
-  l += rowsum;
+  l = l * alpha + rowsum;
 }
 
 __device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
@@ -478,6 +508,62 @@ __device__ __forceinline__ uint4 ld_mask16(const uint32_t* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
+}
+
+// What one CTA owns: a head, a pair of 128-row query tiles and (split mode) a key
+// partition, its key range and the key tiles each query tile needs before any mask
+// skipping.  CTA index -> (head, pair, partition) in groups of kHeadGroup heads, pairs
+// longest first when causal.
+struct CtaPlan {
+  int bh, pair, part, kv_lo, kv_hi, row0_0, row0_1, nkv0, nkv1;
+};
+template <int BM, int BN>
+__device__ __forceinline__ CtaPlan cta_plan(long long idx, int BH, int N, int Nkv, int causal, int nparts, int chunk,
+                                            bool split) {
+  CtaPlan c;
+  const int npairs = (N + 2 * BM - 1) / (2 * BM);
+  c.part = (int)(idx % nparts);
+  idx /= nparts;
+  const int group = (int)(idx / ((long long)kHeadGroup * npairs));
+  const int gheads = min(kHeadGroup, BH - group * kHeadGroup);
+  const int within = (int)(idx - (long long)group * kHeadGroup * npairs);
+  const int pair_rank = within / gheads;
+  c.bh = group * kHeadGroup + within % gheads;
+  c.pair = causal ? (npairs - 1 - pair_rank) : pair_rank;
+  c.kv_lo = split ? min(c.part * chunk, Nkv) : 0;
+  c.kv_hi = split ? min(c.kv_lo + chunk, Nkv) : Nkv;
+  c.row0_0 = c.pair * 2 * BM;
+  c.row0_1 = c.row0_0 + BM;
+  // key tiles needed by the query tile starting at row0; 0 if the tile is empty
+  auto tiles_for = [&](int row0) -> int {
+    if (row0 >= N) return 0;
+    const int last_row = min(row0 + BM - 1, N - 1);
+    const int key_end = causal ? min(c.kv_hi, last_row + 1) : c.kv_hi;
+    return key_end > c.kv_lo ? (key_end - c.kv_lo + BN - 1) / BN : 0;
+  };
+  c.nkv0 = tiles_for(c.row0_0);
+  c.nkv1 = tiles_for(c.row0_1);
+  return c;
+}
+
+// ptxas keeps every value that is live across a setmaxnreg in local memory.  So each
+// role derives what it needs again after its setmaxnreg, from sources that are not
+// registers: the thread and CTA indices (read afresh, so the compiler cannot reuse the
+// earlier reads), the kernel parameters and shared memory.
+__device__ __forceinline__ int tid_fresh() {
+  int v;
+  asm volatile("mov.u32 %0, %%tid.x;" : "=r"(v));
+  return v;
+}
+__device__ __forceinline__ int ctaid_fresh() {
+  int v;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(v));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_fresh(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+  return v;
 }
 
 template <int D, int BN, bool BF16, bool MASK, bool SPLIT>
@@ -516,33 +602,10 @@ __global__ void __launch_bounds__(384, 1)
   // ---- which query tiles, head and key range this CTA owns
   constexpr bool split = SPLIT;  // split-K partitions (P > 0) or the plain forward
   const int nparts = split ? P : 1;
-  const int npairs = (N + 2 * BM - 1) / (2 * BM);
-  // CTA index -> (head, query-tile pair, partition): groups of kHeadGroup heads, pairs
-  // longest first when causal.
-  auto cta_coords = [&](long long idx, int& bh_, int& pair_, int& part_) {
-    part_ = (int)(idx % nparts);
-    idx /= nparts;
-    const int group = (int)(idx / ((long long)kHeadGroup * npairs));
-    const int gheads = min(kHeadGroup, BH - group * kHeadGroup);
-    const int within = (int)(idx - (long long)group * kHeadGroup * npairs);
-    const int pair_rank = within / gheads;
-    bh_ = group * kHeadGroup + within % gheads;
-    pair_ = causal ? (npairs - 1 - pair_rank) : pair_rank;
-  };
-  int bh, pair, part;
-  cta_coords(blockIdx.x, bh, pair, part);
-  const int kv_lo = split ? min(part * chunk, Nkv) : 0;
-  const int kv_hi = split ? min(kv_lo + chunk, Nkv) : Nkv;
-
-  // Key tiles needed by the query tile starting at row0; 0 if the tile is empty.
-  auto tiles_for = [&](int row0) -> int {
-    if (row0 >= N) return 0;
-    const int last_row = min(row0 + BM - 1, N - 1);
-    const int key_end = causal ? min(kv_hi, last_row + 1) : kv_hi;
-    return key_end > kv_lo ? (key_end - kv_lo + BN - 1) / BN : 0;
-  };
-  const int row0_0 = pair * 2 * BM, row0_1 = row0_0 + BM;
-  const int nkv0_all = tiles_for(row0_0), nkv1_all = tiles_for(row0_1);
+  const CtaPlan pl = cta_plan<BM, BN>(blockIdx.x, BH, N, Nkv, causal, nparts, chunk, split);
+  const int bh = pl.bh, kv_lo = pl.kv_lo;
+  const int row0_0 = pl.row0_0, row0_1 = pl.row0_1;
+  const int nkv0_all = pl.nkv0, nkv1_all = pl.nkv1;
   const int nkv_all = max(nkv0_all, nkv1_all);  // key tiles in range, before any skipping
   // With the optional mask, key tiles that no row of this CTA sees are skipped by every
   // role.  They are only known after the set-up, so only the first key tile (always
@@ -603,7 +666,6 @@ __global__ void __launch_bounds__(384, 1)
   // reach are not looked at), then every role counts and walks the
   // marked tiles only (tile 0 is always marked: it is already on its way).  A skipped
   // tile has no visible key for any row of the CTA, so leaving it out changes no result.
-  int nkv0 = nkv0_all, nkv1 = nkv1_all;
   if constexpr (MASK) {
     if (skip) {
       if (warp < 8) {
@@ -637,27 +699,40 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       __syncthreads();
-      nkv0 = count_marked(s_need, nkv0_all);
-      nkv1 = count_marked(s_need, nkv1_all);
     }
   }
-  const int nkv_max = max(nkv0, nkv1);
 
   // Registers move from the copy/MMA warpgroup to the softmax warpgroups.  Each
   // setmaxnreg sits at the top of its role's branch so that the register allocator
   // sees the new limit for all of that role's code.
   if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER) : "memory");
+    // Everything the role uses, derived again after setmaxnreg (see tid_fresh).
+    const int tid = tid_fresh();
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const CtaPlan pl = cta_plan<BM, BN>(ctaid_fresh(), BH, N, Nkv, causal, nparts, chunk, split);
+    const int bh = pl.bh, pair = pl.pair, part = pl.part, kv_lo = pl.kv_lo, kv_hi = pl.kv_hi;
+    const int row0_0 = pl.row0_0, row0_1 = pl.row0_1;
+    const int nkv_all = max(pl.nkv0, pl.nkv1);
+    const bool skip = MASK && nkv_all <= 32 * kNeedWords;
+    const int first = min(skip ? 2 : NSLOT, 2 * nkv_all);
+    const int nkv0 = (MASK && skip) ? count_marked(s_need, pl.nkv0) : pl.nkv0;
+    const int nkv1 = (MASK && skip) ? count_marked(s_need, pl.nkv1) : pl.nkv1;
+    const int nkv_max = max(nkv0, nkv1);
+    const uint32_t tmem = lds_fresh(&s_tmem);
+    (void)pair; (void)part; (void)kv_hi; (void)row0_0; (void)row0_1; (void)first; (void)lane;
+
     if (warp == 8 && lane == 0 && nkv_all > 0) {
       // ============================================================== TMA producer
       // Warm L2 with the Q tiles of the CTA `ahead` launches later (one wave on), which
       // is about when this SM or another picks it up: its first loads then hit L2.
-      if (ahead > 0 && (long long)blockIdx.x + ahead < (long long)gridDim.x) {
-        int bh2, pair2, part2;
-        cta_coords((long long)blockIdx.x + ahead, bh2, pair2, part2);
+      if (ahead > 0 && (long long)ctaid_fresh() + ahead < (long long)gridDim.x) {
+        const CtaPlan ahead_pl = cta_plan<BM, BN>((long long)ctaid_fresh() + ahead, BH, N, Nkv, causal, nparts, chunk,
+                                                  split);
         for (int t = 0; t < 2; ++t)
-          if (pair2 * 2 * BM + t * BM < N)
-            for (int c = 0; c < C::NCH; ++c) tma_prefetch_3d(&tm_q, c * C::CH, pair2 * 2 * BM + t * BM, bh2);
+          if (ahead_pl.row0_0 + t * BM < N)
+            for (int c = 0; c < C::NCH; ++c) tma_prefetch_3d(&tm_q, c * C::CH, ahead_pl.row0_0 + t * BM, ahead_pl.bh);
       }
       int issued = first;
       int ktile = first > 0 ? 0 : -1;  // masked instances: the marked key tile of K/V load n
@@ -683,45 +758,55 @@ __global__ void __launch_bounds__(384, 1)
       mbar_drain(&bar_q, 0, status);
       for (int n = max(0, issued - NSLOT); n < issued; ++n)
         mbar_drain(&bar_full[n % NSLOT], (uint32_t)(n / NSLOT) & 1u, status);
-    } else if (warp == 9 && lane == 0 && nkv_max > 0) {
+    } else if (warp == 9 && nkv_max > 0) {
       // ============================================================== MMA issuer
+      // Every lane walks the loop and waits; the elected lane issues MMAs and commits.
+      const bool leader = elect_one_lane();
       const uint32_t q_addr0 = smem_u32(smem), q_addr1 = q_addr0 + C::Q_BYTES;
       const uint32_t kv_addr = smem_u32(sKV);
-      bool ok = mbar_wait(&bar_q, 0, abort, status, kErrWaitFull);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_q, 0, abort, status, kErrWaitFull));
       int k_ready = -1;
       if (ok && nkv0 > 0) {
-        ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
-        if (ok) issue_qk<C, BF16>(tmem, q_addr0, kv_addr, 0, 0, &bar_s[0]);
+        ok = __all_sync(0xffffffffu, wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status));
+        if (ok && leader) issue_qk<C, BF16>(tmem, q_addr0, kv_addr, 0, 0, &bar_s[0]);
       }
       if (ok && nkv1 > 0) {
-        ok = wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status);
-        if (ok) issue_qk<C, BF16>(tmem, q_addr1, kv_addr, 1, 0, &bar_s[1]);
+        ok = __all_sync(0xffffffffu, wait_kv<NSLOT>(bar_full, 0, k_ready, abort, status));
+        if (ok && leader) issue_qk<C, BF16>(tmem, q_addr1, kv_addr, 1, 0, &bar_s[1]);
       }
-      if (ok) tc_commit(&bar_empty[0]);  // K_0 is free once both S(0) are done
+      if (ok && leader) tc_commit(&bar_empty[0]);  // K_0 is free once both S(0) are done
+      __syncwarp();
       for (int j = 0; ok && j < nkv_max; ++j) {
         for (int t = 0; t < 2; ++t) {
           const int nkv_t = t ? nkv1 : nkv0;
           if (j >= nkv_t) continue;
-          ok = mbar_wait(&bar_p[t], (uint32_t)j & 1u, abort, status, kErrWaitP);
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p[t], (uint32_t)j & 1u, abort, status, kErrWaitP));
           if (!ok) break;
-          issue_pv<C, BF16>(tmem, kv_addr, t, j);
-          if (j == nkv_t - 1) tc_commit(&bar_o[t]);
-          if (j + 1 < nkv_t) issue_qk<C, BF16>(tmem, t ? q_addr1 : q_addr0, kv_addr, t, j + 1, &bar_s[t]);
+          if (leader) {
+            issue_pv<C, BF16>(tmem, kv_addr, t, j);
+            if (j == nkv_t - 1) tc_commit(&bar_o[t]);
+            if (j + 1 < nkv_t) issue_qk<C, BF16>(tmem, t ? q_addr1 : q_addr0, kv_addr, t, j + 1, &bar_s[t]);
+          }
+          __syncwarp();
         }
         if (!ok) break;
-        tc_commit(&bar_empty[(2 * j + 1) % NSLOT]);                      // V_j consumed
-        if (j + 1 < nkv_max) tc_commit(&bar_empty[(2 * j + 2) % NSLOT]);  // K_{j+1} consumed
+        if (leader) {
+          tc_commit(&bar_empty[(2 * j + 1) % NSLOT]);                      // V_j consumed
+          if (j + 1 < nkv_max) tc_commit(&bar_empty[(2 * j + 2) % NSLOT]);  // K_{j+1} consumed
+        }
+        __syncwarp();
       }
-      // Drain every MMA this thread issued before TMEM is released.
-      tc_commit(&bar_done);
-      mbar_drain(&bar_done, 0, status);
+      // Drain every MMA this warp issued before TMEM is released.
+      if (leader) {
+        tc_commit(&bar_done);
+        mbar_drain(&bar_done, 0, status);
+      }
+      __syncwarp();
     } else if (warp == 10 && lane == 0 && nkv_max > 0) {
       // ============================================================== K/V watcher
       // Waits for the copies of V_j and K_(j+1) and adds one arrival to bar_p[t], so
       // that the MMA issuer needs a single wait (P_t(j) written and its operands
-      // loaded) before PV_t(j) and S_t(j+1): every wait the issuing thread makes costs
-      // ~150-200 cycles while the tensor pipe reads shared memory, and the issuer is
-      // on the critical path.
+      // loaded) before PV_t(j) and S_t(j+1): the issuer is on the critical path.
       bool ok = true;
       for (int j = 0; ok && j < nkv_max; ++j)
         for (int t = 0; ok && t < 2; ++t) {
@@ -740,7 +825,23 @@ __global__ void __launch_bounds__(384, 1)
     }
     // warp 11 and the other lanes: nothing to do (they donate registers)
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX) : "memory");
+    // Everything the role uses, derived again after setmaxnreg (see tid_fresh).
+    const int tid = tid_fresh();
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const CtaPlan pl = cta_plan<BM, BN>(ctaid_fresh(), BH, N, Nkv, causal, nparts, chunk, split);
+    const int bh = pl.bh, pair = pl.pair, part = pl.part, kv_lo = pl.kv_lo, kv_hi = pl.kv_hi;
+    const int row0_0 = pl.row0_0, row0_1 = pl.row0_1;
+    const int nkv_all = max(pl.nkv0, pl.nkv1);
+    const bool skip = MASK && nkv_all <= 32 * kNeedWords;
+    const int first = min(skip ? 2 : NSLOT, 2 * nkv_all);
+    const int nkv0 = (MASK && skip) ? count_marked(s_need, pl.nkv0) : pl.nkv0;
+    const int nkv1 = (MASK && skip) ? count_marked(s_need, pl.nkv1) : pl.nkv1;
+    const int nkv_max = max(nkv0, nkv1);
+    const uint32_t tmem = lds_fresh(&s_tmem);
+    (void)pair; (void)part; (void)kv_hi; (void)row0_0; (void)row0_1; (void)first; (void)lane;
+
     // ================================================================ softmax warpgroups
     const int t = warp >> 2;    // query tile of this warpgroup
     const int quad = warp & 3;  // TMEM lane quadrant = rows 32*quad .. 32*quad+31
@@ -863,7 +964,7 @@ __global__ void __launch_bounds__(384, 1)
       // the last CTA's thread 0 fences again (acquire) before the barrier that releases
       // the merge.
       named_bar_sync(3, 256);
-      const long long g = (long long)bh * npairs + pair;
+      const long long g = (long long)bh * ((N + 2 * BM - 1) / (2 * BM)) + pair;
       if (tid == 0) {
         fence_acq_rel_gpu();
         s_last = atomicAdd(fm.counters + g, 1u) == (unsigned)(P - 1);
@@ -883,9 +984,9 @@ __global__ void __launch_bounds__(384, 1)
   // ---- tear-down: everyone is done with TMEM before it is released
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if ((tid_fresh() >> 5) == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tmem_dealloc(lds_fresh(&s_tmem), C::TMEM_COLS);
   }
 }
 

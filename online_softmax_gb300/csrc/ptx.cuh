@@ -222,6 +222,13 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// True in exactly one lane of the (fully converged) warp.
+__device__ __forceinline__ bool elect_one_lane() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 // 2^x with the MUFU approximation; results below 2^-126 flush to +0 (ftz), which costs
 // nothing here (such weights are far below FP32 resolution of any running sum) and
 // keeps the instruction a single MUFU operation.
