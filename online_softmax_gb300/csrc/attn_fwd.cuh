@@ -228,16 +228,16 @@ __device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) {
   return ((uint64_t)hi << 32) | lo;
 }
 
-// S_t = Q_t K_j^T: D/16 MMAs of K = 16 (32 bytes of each operand row), walking the
-// swizzled row chunks.
+// S_t = Q_t K^T with K in ring entry `entry`: D/16 MMAs of K = 16 (32 bytes of each
+// operand row), walking the swizzled row chunks.
 template <class C, bool BF16>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t q_addr, uint32_t kv_addr, int t, int j,
-                                         uint64_t* bar) {
+__device__ __forceinline__ void issue_qk_e(uint32_t tmem, uint32_t q_addr, uint32_t kv_addr, int t, int entry,
+                                           uint64_t* bar) {
   constexpr uint32_t IDESC = idesc_f16(128, C::BN_, BF16, false);
   constexpr int KPC = C::CH / 16;  // K steps per row chunk
   const uint32_t hi = desc_hi<C>();
   const uint32_t a0 = desc_lo(q_addr, 16);
-  const uint32_t b0 = desc_lo(kv_addr + ((2 * j) % C::NSLOT) * C::KV_BYTES, 16);
+  const uint32_t b0 = desc_lo(kv_addr + (entry % C::NSLOT) * C::KV_BYTES, 16);
   const uint32_t d = tmem + (t ? C::COL_S1 : C::COL_S0);
   tc_fence_after();
 #pragma unroll
@@ -249,21 +249,33 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t q_addr, uint32_
   }
   tc_commit(bar);
 }
-
-// O_t += P_t V_j: BN/16 MMAs of K = 16 keys, P read from TMEM (8 packed columns per
-// step), V read MN-major (16 key rows per step; the leading byte offset steps between
-// the 64-column chunks of D).
+// K_j sits in ring entry 2j.
 template <class C, bool BF16>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t kv_addr, int t, int j) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t q_addr, uint32_t kv_addr, int t, int j,
+                                         uint64_t* bar) {
+  issue_qk_e<C, BF16>(tmem, q_addr, kv_addr, t, 2 * j, bar);
+}
+
+// O_t (+)= P_t V with V in ring entry `entry`: BN/16 MMAs of K = 16 keys, P read from
+// TMEM (8 packed columns per step), V read MN-major (16 key rows per step; the leading
+// byte offset steps between the 64-column chunks of D).  `acc` = O already holds
+// earlier tiles.
+template <class C, bool BF16>
+__device__ __forceinline__ void issue_pv_e(uint32_t tmem, uint32_t kv_addr, int t, int entry, bool acc) {
   constexpr uint32_t IDESC = idesc_f16(128, C::D_, BF16, true);
   const uint32_t hi = desc_hi<C>();
-  const uint32_t b0 = desc_lo(kv_addr + ((2 * j + 1) % C::NSLOT) * C::KV_BYTES, C::BN_ * C::SW);
+  const uint32_t b0 = desc_lo(kv_addr + (entry % C::NSLOT) * C::KV_BYTES, C::BN_ * C::SW);
   const uint32_t d = tmem + (t ? C::COL_O1 : C::COL_O0);
   const uint32_t p = tmem + (t ? C::COL_S1 : C::COL_S0);
   tc_fence_after();
 #pragma unroll
   for (int kb = 0; kb < C::BN_ / 16; ++kb)
-    mma_ts_lo(d, p + kb * 8, b0 + ((kb * 16 * C::SW) >> 4), hi, IDESC, (j > 0 || kb > 0) ? 1u : 0u);
+    mma_ts_lo(d, p + kb * 8, b0 + ((kb * 16 * C::SW) >> 4), hi, IDESC, (acc || kb > 0) ? 1u : 0u);
+}
+// V_j sits in ring entry 2j + 1.
+template <class C, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t kv_addr, int t, int j) {
+  issue_pv_e<C, BF16>(tmem, kv_addr, t, 2 * j + 1, j > 0);
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
@@ -657,7 +669,6 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global access
-  const uint32_t tmem = s_tmem;
   volatile int* abort = &s_abort;
 
   // Masked instances: the softmax warps mark every key tile that some row of theirs
@@ -990,6 +1001,366 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// ============================================================================
+// Persistent plain forward (no mask, no split, key tiles of 128).
+//
+// The same warp roles and per-tile code as attn_fwd_kernel, but one CTA per SM walks a
+// list of work items instead of one CTA per item, so the fixed cost of a CTA (set-up,
+// TMEM allocation, the ramp to the first score tile, the tail after the last one and the
+// hand-over of the SM to the next CTA) is paid once per SM: the K/V ring and every
+// barrier's phase run on from one item to the next, the next item's Q tiles are loaded
+// as soon as the current item's last S MMAs have read Q, and its first S MMAs follow
+// the current item's last PV MMAs without a gap.
+//
+// Work units: a unit is one head's query-tile pair, or (causal) the two pairs p and
+// npairs - 1 - p of one head, which together need npairs + 1 key tiles per query tile
+// whatever p is, so that every unit holds the same work; CTA b takes units b, b + G,
+// b + 2G, ... (G = CTAs) in groups of kHeadGroup heads, so the heads in flight keep
+// their K/V in L2.  O leaves through one 32 KB staging tile that the two query tiles
+// use in turn (tile 0 then tile 1 of every item, an empty tile passing its turn).
+struct WorkItem {
+  int bh, row0_0, row0_1, nkv0, nkv1;
+};
+// Item s (0 or 1) of unit u; false when the unit has no such item.
+template <int BM, int BN>
+__device__ __forceinline__ bool unit_item(int u, int s, int BH, int N, int causal, int npairs, int upH,
+                                          WorkItem& it) {
+  const int group = u / (kHeadGroup * upH);
+  const int gheads = min(kHeadGroup, BH - group * kHeadGroup);
+  const int within = u - group * kHeadGroup * upH;
+  const int rank = within / gheads;
+  int pair;
+  if (causal) {
+    const int far = npairs - 1 - rank;  // the longer pair first
+    if (s == 0) pair = far;
+    else if (rank < far) pair = rank;
+    else return false;
+  } else {
+    if (s > 0) return false;
+    pair = rank;
+  }
+  it.bh = group * kHeadGroup + within % gheads;
+  it.row0_0 = pair * 2 * BM;
+  it.row0_1 = it.row0_0 + BM;
+  auto tiles_for = [&](int row0) -> int {
+    if (row0 >= N) return 0;
+    const int last_row = min(row0 + BM - 1, N - 1);
+    const int key_end = causal ? last_row + 1 : N;
+    return (key_end + BN - 1) / BN;
+  };
+  it.nkv0 = tiles_for(it.row0_0);
+  it.nkv1 = tiles_for(it.row0_1);
+  return true;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                            float* __restrict__ lse_out, int BH, int N, int causal, float scale_log2,
+                            unsigned int* status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  using C = AttnCfg<D, 128>;
+  constexpr int BM = C::BM;
+  constexpr int BN = 128;
+  constexpr int NSLOT = C::NSLOT;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_full[NSLOT], bar_empty[NSLOT];
+  __shared__ uint64_t bar_q, bar_qfree, bar_s[2], bar_p[2], bar_o[2], bar_wr[2], bar_stg, bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  uint8_t* sKV = smem + 2 * C::Q_BYTES;
+  uint8_t* stg = sKV + NSLOT * C::KV_BYTES;  // output staging tile (one query tile)
+
+  if ((threadIdx.x >> 5) == 9) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 256) {
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+    }
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_qfree, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 129);  // 128 softmax threads + the K/V watcher
+      mbar_init(&bar_o[t], 1);
+      mbar_init(&bar_wr[t], 128);  // the 128 rows of tile t written to the staging tile
+    }
+    mbar_init(&bar_stg, 1);
+    mbar_init(&bar_done, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // previous grid done and visible
+  volatile int* abort = &s_abort;
+  const int npairs = (N + 2 * BM - 1) / (2 * BM);
+  const int upH = causal ? (npairs + 1) / 2 : npairs;  // units per head
+  const int nunits = BH * upH;
+
+  if ((threadIdx.x >> 5) >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER) : "memory");
+    const int tid = tid_fresh();
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int b0 = ctaid_fresh();
+    const int G = gridDim.x;
+    const uint32_t tmem = lds_fresh(&s_tmem);
+
+    if (warp == 8 && lane == 0) {
+      // ============================================================== TMA producer
+      int n = 0;       // ring loads issued (K_j of an item in entry base + 2j, V_j in base + 2j + 1)
+      int q_armed = 0; // Q phases started
+      bool ok = true;
+      for (int u = b0; ok && u < nunits; u += G) {
+        // warm L2 with the Q tiles of this CTA's next unit
+        if (u + G < nunits)
+          for (int s2 = 0; s2 < 2; ++s2) {
+            WorkItem nx;
+            if (!unit_item<BM, BN>(u + G, s2, BH, N, causal, npairs, upH, nx)) break;
+            for (int t = 0; t < 2; ++t)
+              if ((t ? nx.nkv1 : nx.nkv0) > 0)
+                for (int c = 0; c < C::NCH; ++c) tma_prefetch_3d(&tm_q, c * C::CH, t ? nx.row0_1 : nx.row0_0, nx.bh);
+          }
+        for (int s2 = 0; ok && s2 < 2; ++s2) {
+          WorkItem it;
+          if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
+          const int nkv_max = max(it.nkv0, it.nkv1);
+          if (nkv_max == 0) continue;
+          // Q_t of this item may overwrite the previous item's only once its S MMAs are done
+          if (q_armed > 0) ok = mbar_wait(&bar_qfree, (uint32_t)(q_armed - 1) & 1u, abort, status, kErrWaitLoad);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_q, (it.nkv0 > 0 ? C::Q_BYTES : 0) + (it.nkv1 > 0 ? C::Q_BYTES : 0));
+          ++q_armed;
+          for (int t = 0; t < 2; ++t)
+            if ((t ? it.nkv1 : it.nkv0) > 0)
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? it.row0_1 : it.row0_0,
+                            it.bh);
+          for (int m = 0; m < 2 * nkv_max; ++m, ++n) {
+            const int slot = n % NSLOT;
+            const uint32_t use = n / NSLOT;
+            ok = mbar_wait(&bar_empty[slot], (use & 1u) ^ 1u, abort, status, kErrWaitLoad);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
+            const CUtensorMap* map = (m & 1) ? &tm_v : &tm_k;
+            uint8_t* dst = sKV + slot * C::KV_BYTES;
+            for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * BN * C::SW, map, &bar_full[slot], c * C::CH, (m >> 1) * BN, it.bh);
+          }
+        }
+      }
+      // Drain the copies still in flight before the CTA may exit.
+      if (q_armed > 0) mbar_drain(&bar_q, (uint32_t)(q_armed - 1) & 1u, status);
+      for (int e = max(0, n - NSLOT); e < n; ++e) mbar_drain(&bar_full[e % NSLOT], (uint32_t)(e / NSLOT) & 1u, status);
+    } else if (warp == 9) {
+      // ============================================================== MMA issuer
+      // Every lane walks the loop and waits; the elected lane issues MMAs and commits.
+      const bool leader = elect_one_lane();
+      const uint32_t q_addr0 = smem_u32(smem), q_addr1 = q_addr0 + C::Q_BYTES;
+      const uint32_t kv_addr = smem_u32(sKV);
+      int nb = 0;               // ring entry of the current item's K_0
+      int k = 0;                // items begun
+      int cp0 = 0, cp1 = 0;     // phases of bar_p[0], bar_p[1] consumed
+      bool ok = true;
+      for (int u = b0; ok && u < nunits; u += G) {
+        for (int s2 = 0; ok && s2 < 2; ++s2) {
+          WorkItem it;
+          if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
+          const int nkv0 = it.nkv0, nkv1 = it.nkv1;
+          const int nkv_max = max(nkv0, nkv1);
+          if (nkv_max == 0) continue;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_q, (uint32_t)k & 1u, abort, status, kErrWaitFull));
+          if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[nb % NSLOT], (uint32_t)(nb / NSLOT) & 1u, abort, status,
+                                                   kErrWaitFull));
+          if (!ok) break;
+          if (leader) {
+            if (nkv0 > 0) issue_qk_e<C, BF16>(tmem, q_addr0, kv_addr, 0, nb, &bar_s[0]);
+            if (nkv1 > 0) issue_qk_e<C, BF16>(tmem, q_addr1, kv_addr, 1, nb, &bar_s[1]);
+            tc_commit(&bar_empty[nb % NSLOT]);  // K_0 is free once both S(0) are done
+            if (nkv_max == 1) tc_commit(&bar_qfree);
+          }
+          __syncwarp();
+          for (int j = 0; ok && j < nkv_max; ++j) {
+            for (int t = 0; t < 2; ++t) {
+              const int nkv_t = t ? nkv1 : nkv0;
+              if (j >= nkv_t) continue;
+              const int cp = t ? cp1++ : cp0++;
+              ok = __all_sync(0xffffffffu, mbar_wait(&bar_p[t], (uint32_t)cp & 1u, abort, status, kErrWaitP));
+              if (!ok) break;
+              if (leader) {
+                issue_pv_e<C, BF16>(tmem, kv_addr, t, nb + 2 * j + 1, j > 0);
+                if (j == nkv_t - 1) tc_commit(&bar_o[t]);
+                if (j + 1 < nkv_t) issue_qk_e<C, BF16>(tmem, t ? q_addr1 : q_addr0, kv_addr, t, nb + 2 * j + 2, &bar_s[t]);
+              }
+              __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) {
+              tc_commit(&bar_empty[(nb + 2 * j + 1) % NSLOT]);                      // V_j consumed
+              if (j + 1 < nkv_max) tc_commit(&bar_empty[(nb + 2 * j + 2) % NSLOT]);  // K_{j+1} consumed
+              if (j + 2 == nkv_max) tc_commit(&bar_qfree);  // this item's last S MMAs are issued
+            }
+            __syncwarp();
+          }
+          nb += 2 * nkv_max;
+          ++k;
+        }
+      }
+      // Drain every MMA this warp issued before TMEM is released.
+      if (leader) {
+        tc_commit(&bar_done);
+        mbar_drain(&bar_done, 0, status);
+      }
+      __syncwarp();
+    } else if (warp == 10 && lane == 0) {
+      // ============================================================== K/V watcher
+      // One arrival on bar_p[t] per group once V_j and K_(j+1) have landed, never for a
+      // phase before the previous phase of bar_p[t] completed (see attn_fwd_kernel).
+      int nb = 0, cp0 = 0, cp1 = 0;
+      bool ok = true;
+      for (int u = b0; ok && u < nunits; u += G) {
+        for (int s2 = 0; ok && s2 < 2; ++s2) {
+          WorkItem it;
+          if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
+          const int nkv_max = max(it.nkv0, it.nkv1);
+          if (nkv_max == 0) continue;
+          for (int j = 0; ok && j < nkv_max; ++j)
+            for (int t = 0; ok && t < 2; ++t) {
+              const int nkv_t = t ? it.nkv1 : it.nkv0;
+              if (j >= nkv_t) continue;
+              const int cp = t ? cp1++ : cp0++;
+              if (cp > 0) ok = mbar_wait(&bar_p[t], (uint32_t)(cp - 1) & 1u, abort, status, kErrWaitP);
+              const int ev = nb + 2 * j + 1;
+              if (ok) ok = mbar_wait(&bar_full[ev % NSLOT], (uint32_t)(ev / NSLOT) & 1u, abort, status, kErrWaitFull);
+              if (ok && j + 1 < nkv_t) {
+                const int ek = nb + 2 * j + 2;
+                ok = mbar_wait(&bar_full[ek % NSLOT], (uint32_t)(ek / NSLOT) & 1u, abort, status, kErrWaitFull);
+              }
+              if (ok) mbar_arrive(&bar_p[t]);
+            }
+          nb += 2 * nkv_max;
+        }
+      }
+    }
+    // warp 11 and the other lanes: nothing to do (they donate registers)
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX) : "memory");
+    // ================================================================ softmax warpgroups
+    const int tid = tid_fresh();
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int b0 = ctaid_fresh();
+    const int G = gridDim.x;
+    const int t = warp >> 2;    // query tile of this warpgroup
+    const int quad = warp & 3;  // TMEM lane quadrant = rows 32*quad .. 32*quad+31
+    const int r = quad * 32 + lane;
+    const uint32_t trow = lds_fresh(&s_tmem) + ((uint32_t)(quad * 32) << 16);
+    const uint32_t col_s = t ? C::COL_S1 : C::COL_S0;
+    const uint32_t col_o = t ? C::COL_O1 : C::COL_O0;
+    const uint4 all_keys = make_uint4(~0u, ~0u, ~0u, ~0u);
+    int cs = 0;  // phases of bar_s[t] consumed
+    int co = 0;  // phases of bar_o[t] consumed
+    int turn = 0;  // staging turns passed (two per item: tile 0, then tile 1)
+    int cw = 0;    // phases of bar_wr[t] consumed
+    bool ok = true;
+    for (int u = b0; ok && u < nunits; u += G) {
+      for (int s2 = 0; ok && s2 < 2; ++s2) {
+        WorkItem it;
+        if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
+        if (max(it.nkv0, it.nkv1) == 0) continue;
+        const int nkv = t ? it.nkv1 : it.nkv0;
+        const int row0 = t ? it.row0_1 : it.row0_0;
+        const int row = row0 + r;
+        float m = -INFINITY;  // running max in use, log2 units of scale*s
+        float l = 0.f;
+        for (int j = 0; j < nkv; ++j) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], (uint32_t)cs & 1u, abort, status, kErrWaitS));
+          ++cs;
+          if (!ok) break;
+          tc_fence_after();
+          softmax_tile<C, BF16, false>(trow, col_s, col_o, j > 0, j * BN, row, row0, N, causal, scale_log2, all_keys, m,
+                                       l);
+          tc_fence_before();
+          mbar_arrive(&bar_p[t]);
+        }
+        if (!ok) break;
+        if (nkv > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[t], (uint32_t)co & 1u, abort, status, kErrWaitO));
+          ++co;
+        }
+        // the staging tile is free once the previous turn's store has read it
+        const int my_turn = turn + t;
+        if (ok && my_turn > 0)
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_stg, (uint32_t)(my_turn - 1) & 1u, abort, status, kErrWaitO));
+        if (!ok) break;
+        if (nkv > 0) {
+          tc_fence_after();
+          const float inv = (l > 0.f) ? 1.f / l : 0.f;
+          constexpr int W = D % 32 == 0 ? 32 : 16;
+#pragma unroll
+          for (int c = 0; c < D / W; ++c) {
+            uint32_t uo[W];
+            tmem_load_cols<W>(trow + col_o + c * W, uo);
+            uint32_t w[W / 2];
+#pragma unroll
+            for (int i = 0; i < W / 2; ++i)
+              w[i] = pack2<BF16>(__uint_as_float(uo[2 * i]) * inv + 0.f, __uint_as_float(uo[2 * i + 1]) * inv + 0.f);
+#pragma unroll
+            for (int v16 = 0; v16 < W / 8; ++v16) {
+              const int col = c * W + v16 * 8;
+              const int ch = col / C::CH;
+              const int unit = (col % C::CH) / 8;
+              *reinterpret_cast<uint4*>(stg + ch * BM * C::SW + swizzled<C::SW>(r, unit)) =
+                  make_uint4(w[4 * v16], w[4 * v16 + 1], w[4 * v16 + 2], w[4 * v16 + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bar_wr[t]);  // this row is in the staging tile
+          if (r == 0) {
+            // all 128 rows written (a bounded wait, unlike a named barrier): store the tile
+            ok = mbar_wait(&bar_wr[t], (uint32_t)cw & 1u, abort, status, kErrWaitO);
+            if (ok && *abort == 0) {
+              for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, stg + c * BM * C::SW, c * C::CH, row0, it.bh);
+              bulk_commit_group();
+              bulk_wait_group_read_0();
+            }
+            mbar_arrive(&bar_stg);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);  // lane 0 of quadrant 0 decided for its warp
+          ++cw;
+          if (row < N && lse_out != nullptr) {
+            const float lse2 = (l > 0.f) ? m + lg2(l) : -INFINITY;
+            lse_out[(size_t)it.bh * N + row] = lse2 * kLn2;
+          }
+        } else if (r == 0) {
+          mbar_arrive(&bar_stg);  // an empty tile passes its turn
+        }
+        turn += 2;
+        if (!ok) break;
+      }
+    }
+    // the stores issued by this warpgroup complete before the grid does
+  }
+
+  // ---- tear-down: everyone is done with TMEM before it is released
+  tc_fence_before();
+  __syncthreads();
+  if ((tid_fresh() >> 5) == 9) {
+    tc_fence_after();
+    tmem_dealloc(lds_fresh(&s_tmem), C::TMEM_COLS);
+  }
+}
+
 // Streaming multiprocessors of the current device (0 if it cannot be queried).
 inline int sm_count() {
   int dev = 0, n = 0;
@@ -1041,9 +1412,56 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The plain forward with key tiles of 128 runs persistent (one CTA per SM walking the
+// work units); the other instances launch one CTA per query-tile pair.
+constexpr bool kPersistentForward = true;
+
+template <int D, bool BF16>
+cudaError_t launch_persist(const AttnArgs& a, cudaStream_t st) {
+  using C = AttnCfg<D, 128>;
+  constexpr int SMEM = C::SMEM_BYTES + C::Q_BYTES;  // + the output staging tile
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  auto kern = attn_fwd_persist_kernel<D, BF16>;
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0 || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < C::REGS_LAUNCH) return cudaErrorInvalidConfiguration;  // see launch_attn_inst
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit, std::memory_order_release);
+  }
+  const long long npairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
+  const long long units = (a.causal ? (npairs + 1) / 2 : npairs) * a.BH;
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int sms = sm_count();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units < sms ? units : (sms > 0 ? sms : 1)));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.BH, a.N, a.causal, a.scale_log2,
+                         a.status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t st) {
   const bool mask = a.mask.bits != nullptr;
+  if (kPersistentForward && a.P == 0 && !mask && block_n == 128)
+    return bf16 ? launch_persist<D, true>(a, st) : launch_persist<D, false>(a, st);
   if (a.P > 0) {  // split-K partitions: key tiles of 128
     if (block_n != 128) return cudaErrorInvalidValue;
     if (mask)
