@@ -425,7 +425,7 @@ def measure_attn(torch, ops, sc, synth, args, world, dev, pk, pk_kind, rank):
                    "parallelism": "replicas" if world == 1 else f"replicas x{world} (independent batches)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
-                     "peak_source": f"{pk_kind} (dense bf16 burst)", "kernel": "attn_fwd_kernel<128,128,bf16>",
+                     "peak_source": f"{pk_kind} (dense bf16 burst)", "kernel": "attn_fwd_persist_kernel<128,bf16>",
                      **clock_aware_roofline(achieved, pk, clocks,
                                              torch.cuda.get_device_properties(dev).multi_processor_count,
                                              peak_run_mhz())},
