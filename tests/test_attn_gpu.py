@@ -70,6 +70,18 @@ def test_default_tile_multihead_ragged(D, causal):
     check_full(qb, kb, vb, "bf16", causal, what=f"D{D} multihead")
 
 
+# attn_fwd runs one CTA per SM walking work units (a query-tile pair, or for causal the
+# pairs p and npairs-1-p of one head) in groups of 8 heads.  These shapes give an odd
+# number of pairs (a unit holding the middle pair alone), a last pair whose second query
+# tile is past the end (N % 256 <= 128), head counts that are not a multiple of 8 and
+# more units than SMs; every row is compared with the oracle.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hh,N,D", [(1, 37, 1100, 64), (2, 19, 2000, 128), (3, 5, 130, 32)])
+def test_persistent_work_units(B, Hh, N, D, causal):
+    qb, kb, vb = H.qkv_host(41 + N % 13, B, Hh, N, D, "bf16")
+    check_full(qb, kb, vb, "bf16", causal, what=f"B{B} H{Hh} N{N} D{D} c{causal}")
+
+
 @pytest.mark.parametrize("block_n", [32, 64, 128])
 def test_d128_tiles_and_scale(block_n):
     qb, kb, vb = H.qkv_host(8, 1, 2, 700, 128, "f16")
