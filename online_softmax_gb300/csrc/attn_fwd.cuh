@@ -1013,8 +1013,8 @@ __global__ void __launch_bounds__(384, 1)
 // the current item's last PV MMAs without a gap.
 //
 // Work units: a unit is one head's query-tile pair, or (causal) the two pairs p and
-// npairs - 1 - p of one head, which together need npairs + 1 key tiles per query tile
-// whatever p is, so that every unit holds the same work; CTA b takes units b, b + G,
+// npairs - 1 - p of one head, which together take 2 npairs + 2 key-tile iterations
+// whatever p is (N a multiple of 256), so that every unit holds the same work; CTA b takes units b, b + G,
 // b + 2G, ... (G = CTAs) in groups of kHeadGroup heads, so the heads in flight keep
 // their K/V in L2.  O leaves through one 32 KB staging tile that the two query tiles
 // use in turn (tile 0 then tile 1 of every item, an empty tile passing its turn).
@@ -1412,10 +1412,6 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The plain forward with key tiles of 128 runs persistent (one CTA per SM walking the
-// work units); the other instances launch one CTA per query-tile pair.
-constexpr bool kPersistentForward = true;
-
 template <int D, bool BF16>
 cudaError_t launch_persist(const AttnArgs& a, cudaStream_t st) {
   using C = AttnCfg<D, 128>;
@@ -1460,7 +1456,9 @@ cudaError_t launch_persist(const AttnArgs& a, cudaStream_t st) {
 template <int D>
 cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t st) {
   const bool mask = a.mask.bits != nullptr;
-  if (kPersistentForward && a.P == 0 && !mask && block_n == 128)
+  // The plain forward with key tiles of 128 runs persistent (one CTA per SM walking the
+  // work units); the other forms launch one CTA per query-tile pair.
+  if (a.P == 0 && !mask && block_n == 128)
     return bf16 ? launch_persist<D, true>(a, st) : launch_persist<D, false>(a, st);
   if (a.P > 0) {  // split-K partitions: key tiles of 128
     if (block_n != 128) return cudaErrorInvalidValue;
@@ -1475,7 +1473,6 @@ cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t
   switch (block_n) {
     case 32: return bf16 ? launch_attn_inst<D, 32, true>(a, st) : launch_attn_inst<D, 32, false>(a, st);
     case 64: return bf16 ? launch_attn_inst<D, 64, true>(a, st) : launch_attn_inst<D, 64, false>(a, st);
-    case 128: return bf16 ? launch_attn_inst<D, 128, true>(a, st) : launch_attn_inst<D, 128, false>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }
