@@ -501,8 +501,11 @@ def measure_noncausal(torch, ops, q, k, v, pk):
 
 def measure_masked(torch, ops, synth, q, k, v, dev):
     """The optional Boolean mask on the same prefill inputs (causal): one shared N x N
-    mask per recipe, packed once; the kernel still computes every tile the causal rule
-    keeps, so the FLOP count is the unmasked one (dense-equivalent TFLOP/s)."""
+    mask per recipe, packed once and summarised once (attn_mask_blocks); the kernel
+    still computes every tile the causal rule keeps, so the FLOP count is the unmasked
+    one (dense-equivalent TFLOP/s).  `tflops` is attn_fwd_masked_blocks (persistent,
+    walks the summary); `scan_tflops` is attn_fwd_masked (one CTA per query-tile pair,
+    each scanning the mask)."""
     import numpy as np
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -521,12 +524,19 @@ def measure_masked(torch, ops, synth, q, k, v, dev):
         pack = lambda: ops.attn_mask_pack(mt)
         pack_s, _ = time_launches(torch, pack, 5)
         bits = pack()
-        fn = lambda: ops.attn_fwd_masked(q, k, v, o, bits, lse, causal=CAUSAL)
+        summarise = lambda: ops.attn_mask_blocks(bits, B, H, N)
+        summary_s, _ = time_launches(torch, summarise, 5)
+        blocks = summarise()
+        fn = lambda: ops.attn_fwd_masked_blocks(q, k, v, o, bits, blocks, lse, causal=CAUSAL)
+        scan = lambda: ops.attn_fwd_masked(q, k, v, o, bits, lse, causal=CAUSAL)
         for _ in range(3):
             fn()
+            scan()
         med, _ = time_launches(torch, fn, 20)
+        med_scan, _ = time_launches(torch, scan, 20)
         out["results"].append({"mask": name, "tflops": FLOPS / med / 1e12, "vs_unmasked": base / med,
-                               "pack_us": pack_s * 1e6})
+                               "scan_tflops": FLOPS / med_scan / 1e12, "scan_vs_unmasked": base / med_scan,
+                               "pack_us": pack_s * 1e6, "summary_us": summary_s * 1e6})
     assert ops.device_error() == 0
     return out
 

@@ -234,6 +234,52 @@ OATTN_API oattn_status attn_fwd_masked(const void* q, const void* k, const void*
                                        long long mask_stride_q, struct CUstream_st* stream);
 
 /*
+ * The block summary of a packed mask: one bit per (mask head, block of 256 query rows,
+ * key tile of 128 keys), set when some row of the block sees some key of the tile.  A
+ * mask head is (b, h) with b taken as 0 when mask_stride_b == 0 and h taken as 0 when
+ * mask_stride_h == 0 (a shared mask has a shared summary).  The words of mask head
+ * (b, h) and block p are blocks[((b*Hm + h)*ceil(Nq/256) + p)*wpb .. + wpb) with
+ * Hm = (mask_stride_h ? H : 1) and wpb = ceil(ceil(Nkv/128)/32); bit j of word i stands
+ * for key tile 32*i + j.  The summary depends only on the mask: it is made once per mask
+ * (as the packing is) and serves every call that uses that mask.
+ *
+ * attn_mask_blocks_words - words of the summary: (mask_stride_b ? B : 1) *
+ *   (mask_stride_h ? H : 1) * ceil(Nq/256) * wpb; 0 when any size is <= 0.
+ */
+OATTN_API long long attn_mask_blocks_words(int B, int H, int Nq, int Nkv, long long mask_stride_b,
+                                           long long mask_stride_h);
+
+/*
+ * attn_mask_blocks - write the block summary of the packed mask (strides as in the
+ *   masked entry points) into `blocks`, a device array of attn_mask_blocks_words(...)
+ *   32-bit words on a 4-byte boundary, owned by the caller; every word is written.  Reads
+ *   rows q < Nq of each mask head.  Nq == 0 or Nkv == 0 is a no-op.  Returns
+ *   OATTN_ERR_INVALID_ARG for negative sizes, null or misaligned pointers and bad
+ *   strides, OATTN_ERR_UNSUPPORTED above 2^31 - 1 summary words.
+ */
+OATTN_API oattn_status attn_mask_blocks(const unsigned int* mask_bits, long long mask_stride_b,
+                                        long long mask_stride_h, long long mask_stride_q, int B, int H,
+                                        int Nq, int Nkv, unsigned int* blocks, struct CUstream_st* stream);
+
+/*
+ * attn_fwd_masked_blocks - attn_fwd_masked with the block summary of the same mask
+ *   (attn_mask_blocks with Nq = Nkv = N, the same pointer, strides, B and H, written
+ *   after the mask's last change; a stale summary leaves out tiles it should not).
+ *   One CTA per SM walks its blocks and visits, in each block, only the key tiles the
+ *   summary marks, so no mask scan precedes the key loop.  When a CTA's share of the
+ *   summary exceeds 256 words (2 * ceil(units / SMs) * wpb, units = B*H*ceil(N/512) for
+ *   causal, B*H*ceil(N/256) otherwise) the call runs as attn_fwd_masked.  Results are
+ *   those of attn_fwd_masked.  Errors as attn_fwd_masked; blocks must be non-NULL and
+ *   4-byte aligned when N > 0.
+ */
+OATTN_API oattn_status attn_fwd_masked_blocks(const void* q, const void* k, const void* v, void* o, float* lse,
+                                              int B, int H, int N, int D, int causal, float scale,
+                                              oattn_dtype dtype, const unsigned int* mask_bits,
+                                              long long mask_stride_b, long long mask_stride_h,
+                                              long long mask_stride_q, const unsigned int* blocks,
+                                              struct CUstream_st* stream);
+
+/*
  * attn_fwd_splitk_masked - attn_fwd_splitk with the optional Boolean mask (above) over
  *   the Nq x Nkv scores of each head.  A (row, partition) whose keys are all hidden
  *   stores O_p = +0 and lse_p = -inf, like an empty partition.  Nq == 1 reads only

@@ -13,6 +13,7 @@ import os
 
 __all__ = ["attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine", "splitk_chunk",
            "attn_mask_words", "attn_mask_pack", "attn_fwd_masked", "attn_fwd_splitk_masked",
+           "attn_mask_blocks_words", "attn_mask_blocks", "attn_fwd_masked_blocks",
            "attn_splitk_counters", "attn_fwd_splitk_fused", "attn_fwd_host",
            "device_error", "OattnError", "library_path", "lib"]
 
@@ -46,6 +47,10 @@ def _load():
     L.attn_mask_words.argtypes = [i]
     L.attn_mask_pack.argtypes = [vp, vp, ll, i, ll, vp]
     L.attn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, ll, ll, vp]
+    L.attn_mask_blocks_words.argtypes = [i, i, i, i, ll, ll]
+    L.attn_mask_blocks_words.restype = ll
+    L.attn_mask_blocks.argtypes = [vp, ll, ll, ll, i, i, i, i, vp, vp]
+    L.attn_fwd_masked_blocks.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, ll, ll, vp, vp]
     L.attn_fwd_splitk_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, i,
                                          vp, ll, ll, ll, vp]
     L.attn_splitk_counters.argtypes = [i, i, i]
@@ -59,7 +64,7 @@ def _load():
     for name in ("attn_fwd", "attn_fwd_bn", "attn_fwd_splitk", "attn_fwd_splitk_noalloc", "splitk_combine",
                  "splitk_chunk", "oattn_device_error", "attn_mask_words", "attn_mask_pack", "attn_fwd_masked",
                  "attn_fwd_splitk_masked", "attn_splitk_counters", "attn_fwd_splitk_fused", "attn_fwd_host",
-                 "oattn_selftest_wait"):
+                 "oattn_selftest_wait", "attn_mask_blocks", "attn_fwd_masked_blocks"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -301,6 +306,47 @@ def attn_fwd_masked(q, k, v, o, mask, lse=None, causal=False, scale=None, stream
     st = lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, int(bool(causal)),
                              scale, _dtype_code(q.dtype), mp, sb, sh, sq, _stream(stream))
     _raise(st, "attn_fwd_masked")
+    return o, lse
+
+
+def attn_mask_blocks_words(B: int, H: int, Nq: int, Nkv: int, stride_b: int, stride_h: int) -> int:
+    """32-bit words of the block summary of a mask with these strides (0 = shared)."""
+    return lib.attn_mask_blocks_words(int(B), int(H), int(Nq), int(Nkv), int(stride_b), int(stride_h))
+
+
+def attn_mask_blocks(mask, B, H, Nq, Nkv=None, blocks=None, stream=None):
+    """Block summary of a mask broadcast against [B, H, Nq, Nkv] (Boolean, or its packed
+    bits): one bit per (mask head, 256 query rows, 128-key tile), set when some row of
+    the block sees some key of the tile.  Returns int32 [attn_mask_blocks_words(...)]."""
+    import torch
+    Nkv = Nq if Nkv is None else Nkv
+    keep, mp, sb, sh, sq = _mask_strides(mask, B, H, Nq, Nkv, stream)
+    n = attn_mask_blocks_words(B, H, Nq, Nkv, sb, sh)
+    if blocks is None:
+        blocks = torch.empty(max(n, 1), dtype=torch.int32, device=keep.device)
+    if blocks.dtype != torch.int32 or not blocks.is_cuda or not blocks.is_contiguous() or blocks.numel() < n:
+        raise ValueError(f"blocks must be a contiguous CUDA int32 tensor of at least {n} words")
+    st = lib.attn_mask_blocks(mp, sb, sh, sq, int(B), int(H), int(Nq), int(Nkv), _ptr(blocks), _stream(stream))
+    _raise(st, "attn_mask_blocks")
+    return blocks
+
+
+def attn_fwd_masked_blocks(q, k, v, o, mask, blocks, lse=None, causal=False, scale=None, stream=None):
+    """attn_fwd_masked with the block summary of the same mask (attn_mask_blocks with
+    the same mask and B, H, Nq = Nkv = N): the persistent kernel visits only the key
+    tiles the summary marks."""
+    import torch
+    B, H, N, D = q.shape
+    _check(q, "q"); _check(k, "k", q.dtype, q.shape); _check(v, "v", q.dtype, q.shape)
+    _check(o, "o", q.dtype, q.shape); _check(lse, "lse", torch.float32, (B, H, N))
+    scale = D ** -0.5 if scale is None else float(scale)
+    keep, mp, sb, sh, sq = _mask_strides(mask, B, H, N, N, stream)
+    n = attn_mask_blocks_words(B, H, N, N, sb, sh)
+    if blocks.dtype != torch.int32 or not blocks.is_cuda or not blocks.is_contiguous() or blocks.numel() < n:
+        raise ValueError(f"blocks must be the summary of this mask: a contiguous CUDA int32 tensor of {n} words")
+    st = lib.attn_fwd_masked_blocks(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, int(bool(causal)),
+                                    scale, _dtype_code(q.dtype), mp, sb, sh, sq, _ptr(blocks), _stream(stream))
+    _raise(st, "attn_fwd_masked_blocks")
     return o, lse
 
 

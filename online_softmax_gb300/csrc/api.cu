@@ -165,7 +165,7 @@ MaskArgs mask_args(const unsigned int* bits, long long sb, long long sh, long lo
 
 oattn_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                            int N, int D, int causal, float scale, oattn_dtype dtype, int block_n,
-                           const MaskArgs& mk, cudaStream_t st) {
+                           const MaskArgs& mk, cudaStream_t st, const MaskBlocks& mblocks = MaskBlocks{}) {
   oattn_status s = attn_common_checks(q, k, v, B, H, N, N, D, scale, dtype);
   if (s != OATTN_OK) return s;
   if (block_n == 0) block_n = 128;
@@ -193,6 +193,7 @@ oattn_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o,
   a.chunk = 0;
   a.out_f32 = 0;
   a.mask = mk;
+  a.mblocks = mblocks;
   return launch_attn(a, block_n, bf16, st) == cudaSuccess ? OATTN_OK : OATTN_ERR_CUDA;
 }
 
@@ -438,6 +439,48 @@ oattn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* 
   return attn_fwd_impl(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, 128,
                        mask_args(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q, H),
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+long long attn_mask_blocks_words(int B, int H, int Nq, int Nkv, long long mask_stride_b, long long mask_stride_h) {
+  return mask_blocks_words(B, H, Nq, Nkv, mask_stride_b, mask_stride_h);
+}
+
+oattn_status attn_mask_blocks(const unsigned int* mask_bits, long long mask_stride_b, long long mask_stride_h,
+                              long long mask_stride_q, int B, int H, int Nq, int Nkv, unsigned int* blocks,
+                              struct CUstream_st* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nkv < 0) return OATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || Nq == 0 || Nkv == 0) return OATTN_OK;
+  const oattn_status s = mask_checks(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q);
+  if (s != OATTN_OK) return s;
+  if (!blocks || !aligned(blocks, 4)) return OATTN_ERR_INVALID_ARG;
+  if (mask_blocks_words(B, H, Nq, Nkv, mask_stride_b, mask_stride_h) > 0x7fffffffLL) return OATTN_ERR_UNSUPPORTED;
+  return launch_mask_blocks(reinterpret_cast<const uint32_t*>(mask_bits), mask_stride_b, mask_stride_h,
+                            mask_stride_q, B, H, Nq, Nkv, reinterpret_cast<uint32_t*>(blocks),
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? OATTN_OK
+             : OATTN_ERR_CUDA;
+}
+
+oattn_status attn_fwd_masked_blocks(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                    int N, int D, int causal, float scale, oattn_dtype dtype,
+                                    const unsigned int* mask_bits, long long mask_stride_b, long long mask_stride_h,
+                                    long long mask_stride_q, const unsigned int* blocks, struct CUstream_st* stream) {
+  MaskBlocks mb{};
+  if (N > 0) {
+    const oattn_status s = mask_checks(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q);
+    if (s != OATTN_OK) return s;
+    if (!blocks || !aligned(blocks, 4)) return OATTN_ERR_INVALID_ARG;
+    const int wpb = mask_block_wpb(N);
+    const long long nblk = (N + 255) / 256;
+    const long long hm = mask_stride_h ? H : 1;
+    mb.bits = reinterpret_cast<const uint32_t*>(blocks);
+    mb.wpb = wpb;
+    mb.sh = mask_stride_h ? nblk * wpb : 0;
+    mb.sb = mask_stride_b ? hm * nblk * wpb : 0;
+  }
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, 128,
+                       mask_args(mask_bits, mask_stride_b, mask_stride_h, mask_stride_q, H),
+                       reinterpret_cast<cudaStream_t>(stream), mb);
 }
 
 oattn_status attn_fwd_splitk_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,

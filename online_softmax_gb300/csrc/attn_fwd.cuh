@@ -376,6 +376,7 @@ __device__ __forceinline__ void merge_row(const void* o_partial, const float* ls
 // [0, n) are marked, and the first marked tile at or after `from` (callers walk at most
 // as many tiles as are marked; past the last word the walk returns the end index).
 constexpr int kNeedWords = 64;  // key tiles a CTA can skip over: 64 * 32 = 2048
+constexpr int kListWords = 256; // persistent masked kernel: summary words of one CTA's items
 __device__ __forceinline__ int count_marked(const uint32_t* need, int n) {
   int c = 0;
   for (int w = 0; w * 32 < n; ++w) {
@@ -385,12 +386,12 @@ __device__ __forceinline__ int count_marked(const uint32_t* need, int n) {
   }
   return c;
 }
-__device__ __forceinline__ int next_marked(const uint32_t* need, int from) {
+__device__ __forceinline__ int next_marked(const uint32_t* need, int from, int nwords = kNeedWords) {
   int w = from >> 5;
-  if (w >= kNeedWords) return kNeedWords * 32;
+  if (w >= nwords) return nwords * 32;
   uint32_t bits = need[w] & (~0u << (from & 31));
   while (bits == 0u) {
-    if (++w >= kNeedWords) return kNeedWords * 32;
+    if (++w >= nwords) return nwords * 32;
     bits = need[w];
   }
   return w * 32 + __ffs(bits) - 1;
@@ -1053,12 +1054,39 @@ __device__ __forceinline__ bool unit_item(int u, int s, int BH, int N, int causa
   return true;
 }
 
-template <int D, bool BF16>
+// Masked form (MASK): the block summary of the mask (one bit per block of 256 query rows
+// and key tile) gives each item the key tiles it visits: marked tiles within its reach,
+// counted and walked alike by every role.  A query tile whose tiles are all unmarked
+// writes o = +0 and lse = -inf for its rows.
+// Item s of the i-th unit of this CTA: its summary words at list + (2 i + s) * wpb (zeros
+// where the unit has no such item).  Not inlined, so that none of its values stays live
+// into the roles (each role re-derives what it needs after setmaxnreg).
+template <int BM, int BN>
+__device__ __noinline__ void fill_item_list(uint32_t* list, int BH, int N, int causal, int H, const uint32_t* bits,
+                                            long long sb, long long sh, int wpb) {
+  const int npairs = (N + 2 * BM - 1) / (2 * BM);
+  const int upH = causal ? (npairs + 1) / 2 : npairs;
+  const int nunits = BH * upH;
+  const int G = gridDim.x;
+  const int nlist = min(2 * ((nunits - (int)blockIdx.x + G - 1) / G) * wpb, kListWords);
+  for (int x = threadIdx.x; x < nlist; x += blockDim.x) {
+    const int i = x / (2 * wpb), s2 = (x / wpb) & 1, w = x % wpb;
+    WorkItem it;
+    uint32_t v = 0u;
+    if (unit_item<BM, BN>((int)blockIdx.x + i * G, s2, BH, N, causal, npairs, upH, it)) {
+      const int b = it.bh / H, h = it.bh - b * H;
+      v = bits[b * sb + h * sh + (long long)(it.row0_0 / (2 * BM)) * wpb + w];
+    }
+    list[x] = v;
+  }
+}
+
+template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                             float* __restrict__ lse_out, int BH, int N, int causal, float scale_log2,
-                            unsigned int* status) {
+                            const MaskArgs mk, const MaskBlocks mb, unsigned int* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using C = AttnCfg<D, 128>;
   constexpr int BM = C::BM;
@@ -1070,6 +1098,7 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ uint64_t bar_q, bar_qfree, bar_s[2], bar_p[2], bar_o[2], bar_wr[2], bar_stg, bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ uint32_t s_list[MASK ? kListWords : 1];  // masked: summary words of this CTA's items
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -1106,6 +1135,12 @@ __global__ void __launch_bounds__(384, 1)
   const int npairs = (N + 2 * BM - 1) / (2 * BM);
   const int upH = causal ? (npairs + 1) / 2 : npairs;  // units per head
   const int nunits = BH * upH;
+  // Masked: item s of this CTA's i-th unit finds its summary words at s_list + (2 i + s)
+  // * wpb (zeros where the unit has no such item); the launch keeps them within the list.
+  if constexpr (MASK) {
+    fill_item_list<BM, BN>(s_list, BH, N, causal, mk.H, mb.bits, mb.sb, mb.sh, mb.wpb);
+    __syncthreads();
+  }
 
   if ((threadIdx.x >> 5) >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_OTHER) : "memory");
@@ -1121,7 +1156,8 @@ __global__ void __launch_bounds__(384, 1)
       int n = 0;       // ring loads issued (K_j of an item in entry base + 2j, V_j in base + 2j + 1)
       int q_armed = 0; // Q phases started
       bool ok = true;
-      for (int u = b0; ok && u < nunits; u += G) {
+      int ui = 0;      // units begun
+      for (int u = b0; ok && u < nunits; u += G, ++ui) {
         // warm L2 with the Q tiles of this CTA's next unit
         if (u + G < nunits)
           for (int s2 = 0; s2 < 2; ++s2) {
@@ -1134,18 +1170,22 @@ __global__ void __launch_bounds__(384, 1)
         for (int s2 = 0; ok && s2 < 2; ++s2) {
           WorkItem it;
           if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
-          const int nkv_max = max(it.nkv0, it.nkv1);
+          const uint32_t* list = s_list + (MASK ? (2 * ui + s2) * mb.wpb : 0);
+          const int nkv0 = MASK ? count_marked(list, it.nkv0) : it.nkv0;
+          const int nkv1 = MASK ? count_marked(list, it.nkv1) : it.nkv1;
+          const int nkv_max = max(nkv0, nkv1);
           if (nkv_max == 0) continue;
           // Q_t of this item may overwrite the previous item's only once its S MMAs are done
           if (q_armed > 0) ok = mbar_wait(&bar_qfree, (uint32_t)(q_armed - 1) & 1u, abort, status, kErrWaitLoad);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bar_q, (it.nkv0 > 0 ? C::Q_BYTES : 0) + (it.nkv1 > 0 ? C::Q_BYTES : 0));
+          mbar_arrive_expect_tx(&bar_q, (nkv0 > 0 ? C::Q_BYTES : 0) + (nkv1 > 0 ? C::Q_BYTES : 0));
           ++q_armed;
           for (int t = 0; t < 2; ++t)
-            if ((t ? it.nkv1 : it.nkv0) > 0)
+            if ((t ? nkv1 : nkv0) > 0)
               for (int c = 0; c < C::NCH; ++c)
                 tma_load_3d(smem + t * C::Q_BYTES + c * BM * C::SW, &tm_q, &bar_q, c * C::CH, t ? it.row0_1 : it.row0_0,
                             it.bh);
+          int ktile = -1;  // key tile of the K/V pair being loaded
           for (int m = 0; m < 2 * nkv_max; ++m, ++n) {
             const int slot = n % NSLOT;
             const uint32_t use = n / NSLOT;
@@ -1153,8 +1193,9 @@ __global__ void __launch_bounds__(384, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(&bar_full[slot], C::KV_BYTES);
             const CUtensorMap* map = (m & 1) ? &tm_v : &tm_k;
+            if ((m & 1) == 0) ktile = MASK ? next_marked(list, ktile + 1, mb.wpb) : m >> 1;
             uint8_t* dst = sKV + slot * C::KV_BYTES;
-            for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * BN * C::SW, map, &bar_full[slot], c * C::CH, (m >> 1) * BN, it.bh);
+            for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * BN * C::SW, map, &bar_full[slot], c * C::CH, ktile * BN, it.bh);
           }
         }
       }
@@ -1171,11 +1212,14 @@ __global__ void __launch_bounds__(384, 1)
       int k = 0;                // items begun
       int cp0 = 0, cp1 = 0;     // phases of bar_p[0], bar_p[1] consumed
       bool ok = true;
-      for (int u = b0; ok && u < nunits; u += G) {
+      int ui = 0;               // units begun
+      for (int u = b0; ok && u < nunits; u += G, ++ui) {
         for (int s2 = 0; ok && s2 < 2; ++s2) {
           WorkItem it;
           if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
-          const int nkv0 = it.nkv0, nkv1 = it.nkv1;
+          const uint32_t* list = s_list + (MASK ? (2 * ui + s2) * mb.wpb : 0);
+          const int nkv0 = MASK ? count_marked(list, it.nkv0) : it.nkv0;
+          const int nkv1 = MASK ? count_marked(list, it.nkv1) : it.nkv1;
           const int nkv_max = max(nkv0, nkv1);
           if (nkv_max == 0) continue;
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_q, (uint32_t)k & 1u, abort, status, kErrWaitFull));
@@ -1228,15 +1272,19 @@ __global__ void __launch_bounds__(384, 1)
       // phase before the previous phase of bar_p[t] completed (see attn_fwd_kernel).
       int nb = 0, cp0 = 0, cp1 = 0;
       bool ok = true;
-      for (int u = b0; ok && u < nunits; u += G) {
+      int ui = 0;  // units begun
+      for (int u = b0; ok && u < nunits; u += G, ++ui) {
         for (int s2 = 0; ok && s2 < 2; ++s2) {
           WorkItem it;
           if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
-          const int nkv_max = max(it.nkv0, it.nkv1);
+          const uint32_t* list = s_list + (MASK ? (2 * ui + s2) * mb.wpb : 0);
+          const int nkv0 = MASK ? count_marked(list, it.nkv0) : it.nkv0;
+          const int nkv1 = MASK ? count_marked(list, it.nkv1) : it.nkv1;
+          const int nkv_max = max(nkv0, nkv1);
           if (nkv_max == 0) continue;
           for (int j = 0; ok && j < nkv_max; ++j)
             for (int t = 0; ok && t < 2; ++t) {
-              const int nkv_t = t ? it.nkv1 : it.nkv0;
+              const int nkv_t = t ? nkv1 : nkv0;
               if (j >= nkv_t) continue;
               const int cp = t ? cp1++ : cp0++;
               if (cp > 0) ok = mbar_wait(&bar_p[t], (uint32_t)(cp - 1) & 1u, abort, status, kErrWaitP);
@@ -1273,23 +1321,35 @@ __global__ void __launch_bounds__(384, 1)
     int turn = 0;  // staging turns passed (two per item: tile 0, then tile 1)
     int cw = 0;    // phases of bar_wr[t] consumed
     bool ok = true;
-    for (int u = b0; ok && u < nunits; u += G) {
+    int ui = 0;  // units begun
+    for (int u = b0; ok && u < nunits; u += G, ++ui) {
       for (int s2 = 0; ok && s2 < 2; ++s2) {
         WorkItem it;
         if (!unit_item<BM, BN>(u, s2, BH, N, causal, npairs, upH, it)) break;
         if (max(it.nkv0, it.nkv1) == 0) continue;
-        const int nkv = t ? it.nkv1 : it.nkv0;
+        const uint32_t* list = s_list + (MASK ? (2 * ui + s2) * mb.wpb : 0);
+        const int reach = t ? it.nkv1 : it.nkv0;  // key tiles before any skipping (0: no rows)
+        const int nkv = MASK ? count_marked(list, reach) : reach;
         const int row0 = t ? it.row0_1 : it.row0_0;
         const int row = row0 + r;
+        // this row's packed mask words (rows past N see every key of the visited tiles)
+        const uint32_t* mrow = nullptr;
+        if (MASK && row < N) {
+          const int b = it.bh / mk.H, h = it.bh - b * mk.H;
+          mrow = mk.bits + b * mk.sb + h * mk.sh + (long long)row * mk.sq;
+        }
         float m = -INFINITY;  // running max in use, log2 units of scale*s
         float l = 0.f;
+        int tj = -1;  // key tile of iteration j
         for (int j = 0; j < nkv; ++j) {
+          tj = MASK ? next_marked(list, tj + 1, mb.wpb) : j;
+          uint4 w = all_keys;
+          if (MASK && mrow != nullptr) w = ld_mask16(mrow + 4 * tj);
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], (uint32_t)cs & 1u, abort, status, kErrWaitS));
           ++cs;
           if (!ok) break;
           tc_fence_after();
-          softmax_tile<C, BF16, false>(trow, col_s, col_o, j > 0, j * BN, row, row0, N, causal, scale_log2, all_keys, m,
-                                       l);
+          softmax_tile<C, BF16, MASK>(trow, col_s, col_o, j > 0, tj * BN, row, row0, N, causal, scale_log2, w, m, l);
           tc_fence_before();
           mbar_arrive(&bar_p[t]);
         }
@@ -1303,14 +1363,19 @@ __global__ void __launch_bounds__(384, 1)
         if (ok && my_turn > 0)
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_stg, (uint32_t)(my_turn - 1) & 1u, abort, status, kErrWaitO));
         if (!ok) break;
-        if (nkv > 0) {
+        if (reach > 0) {
           tc_fence_after();
           const float inv = (l > 0.f) ? 1.f / l : 0.f;
           constexpr int W = D % 32 == 0 ? 32 : 16;
 #pragma unroll
           for (int c = 0; c < D / W; ++c) {
             uint32_t uo[W];
-            tmem_load_cols<W>(trow + col_o + c * W, uo);
+            if (!MASK || nkv > 0) {
+              tmem_load_cols<W>(trow + col_o + c * W, uo);
+            } else {  // every key tile of this query tile was skipped: o = +0
+#pragma unroll
+              for (int i = 0; i < W; ++i) uo[i] = 0u;
+            }
             uint32_t w[W / 2];
 #pragma unroll
             for (int i = 0; i < W / 2; ++i)
@@ -1412,12 +1477,30 @@ cudaError_t launch_attn_inst(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+// Grid of the persistent kernel: one CTA per SM, or one per unit when there are fewer.
+inline long long persist_units(const AttnArgs& a) {
+  const long long npairs = (a.N + 2 * 128LL - 1) / (2 * 128LL);
+  return (a.causal ? (npairs + 1) / 2 : npairs) * a.BH;
+}
+inline int persist_grid(long long units) {
+  const int sms = sm_count();
+  return (int)(units < sms ? units : (sms > 0 ? sms : 1));
+}
+// The masked persistent form keeps the summary words of all of a CTA's items in shared
+// memory: two item slots per unit of the CTA, mblocks.wpb words each.
+inline bool persist_mask_fits(const AttnArgs& a) {
+  const long long units = persist_units(a);
+  if (units <= 0 || a.mblocks.bits == nullptr || a.mblocks.wpb <= 0) return false;
+  const long long g = persist_grid(units);
+  return 2 * ((units + g - 1) / g) * a.mblocks.wpb <= kListWords;
+}
+
+template <int D, bool BF16, bool MASK>
 cudaError_t launch_persist(const AttnArgs& a, cudaStream_t st) {
   using C = AttnCfg<D, 128>;
   constexpr int SMEM = C::SMEM_BYTES + C::Q_BYTES;  // + the output staging tile
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-  auto kern = attn_fwd_persist_kernel<D, BF16>;
+  auto kern = attn_fwd_persist_kernel<D, BF16, MASK>;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1432,13 +1515,12 @@ cudaError_t launch_persist(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  const long long npairs = (a.N + 2 * C::BM - 1) / (2 * C::BM);
-  const long long units = (a.causal ? (npairs + 1) / 2 : npairs) * a.BH;
+  const long long units = persist_units(a);
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const int sms = sm_count();
+  if (MASK && !persist_mask_fits(a)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(units < sms ? units : (sms > 0 ? sms : 1)));
+  cfg.gridDim = dim3((unsigned)persist_grid(units));
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = st;
@@ -1448,7 +1530,7 @@ cudaError_t launch_persist(const AttnArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.BH, a.N, a.causal, a.scale_log2,
-                         a.status);
+                         a.mask, a.mblocks, a.status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1457,9 +1539,12 @@ template <int D>
 cudaError_t launch_attn_d(const AttnArgs& a, int block_n, int bf16, cudaStream_t st) {
   const bool mask = a.mask.bits != nullptr;
   // The plain forward with key tiles of 128 runs persistent (one CTA per SM walking the
-  // work units); the other forms launch one CTA per query-tile pair.
+  // work units), masked too when the mask's block summary is given and fits; the other
+  // forms launch one CTA per query-tile pair.
   if (a.P == 0 && !mask && block_n == 128)
-    return bf16 ? launch_persist<D, true>(a, st) : launch_persist<D, false>(a, st);
+    return bf16 ? launch_persist<D, true, false>(a, st) : launch_persist<D, false, false>(a, st);
+  if (a.P == 0 && mask && block_n == 128 && persist_mask_fits(a))
+    return bf16 ? launch_persist<D, true, true>(a, st) : launch_persist<D, false, true>(a, st);
   if (a.P > 0) {  // split-K partitions: key tiles of 128
     if (block_n != 128) return cudaErrorInvalidValue;
     if (mask)

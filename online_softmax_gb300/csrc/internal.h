@@ -33,6 +33,20 @@ inline int mask_words(int nkv) { return 4 * ((nkv + 127) / 128); }
 cudaError_t launch_mask_pack(const uint8_t* mask, uint32_t* bits, long long rows, int nkv,
                              long long row_stride, cudaStream_t st);
 
+// Block summary of a packed mask (one bit per mask head, block of 256 query rows and key
+// tile of 128: set iff some row of the block sees some key of the tile).  A mask stride of
+// 0 shares the mask, and so its summary, along that axis; the words of (b, h, block p)
+// are bits + b * sb + h * sh + p * wpb.
+struct MaskBlocks {
+  const uint32_t* bits;  // nullptr: no summary
+  long long sb, sh;
+  int wpb;               // words per block
+};
+inline int mask_block_wpb(int nkv) { return ((nkv + 127) / 128 + 31) / 32; }
+long long mask_blocks_words(int B, int H, int nq, int nkv, long long sb, long long sh);
+cudaError_t launch_mask_blocks(const uint32_t* bits, long long sb, long long sh, long long sq, int B, int H, int nq,
+                               int nkv, uint32_t* blocks, cudaStream_t st);
+
 // ---- in-kernel split-K merge: the last CTA to finish a group of P partitions merges
 // them.  counters[g] counts the arrivals of group g (one per row-head in decode, one per
 // (head, pair of query tiles) in the tcgen05 split mode); the last arrival resets it to 0.
@@ -72,6 +86,7 @@ struct AttnArgs {
   int P, chunk;       // split mode when P > 0
   int out_f32;        // split mode: o_partial is float32
   MaskArgs mask;      // optional (key tiles of 128 only)
+  MaskBlocks mblocks; // optional block summary of the mask (plain mode)
   FusedMerge fused;   // split mode: optional in-kernel merge
   unsigned int* status;
 };

@@ -25,7 +25,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:OATTN_API\s+)?(?:oattn_status|int|const char\*)\s+(\w+)\s*\(", text,
+    return sorted(set(re.findall(r"^\s*(?:OATTN_API\s+)?(?:oattn_status|int|long long|const char\*)\s+(\w+)\s*\(", text,
                                  flags=re.M)))
 
 
@@ -194,6 +194,53 @@ def test_mask_pack_rejects(lib, args, expect):
 def test_empty_masked_problems_accept_null_pointers(lib):
     assert masked(lib, q=None, k=None, v=None, o=None, m=None, N=0) == 0
     assert splitk_masked(lib, q=None, k=None, v=None, op=None, lp=None, m=None, Nq=0) == 0
+    assert masked_blocks(lib, q=None, k=None, v=None, o=None, m=None, blocks=None, N=0) == 0
+    assert mask_blocks(lib, m=None, blocks=None, Nq=0) == 0
+    assert mask_blocks(lib, m=None, blocks=None, Nkv=0) == 0
+
+
+# --- the block summary of a mask ------------------------------------------------------
+@pytest.mark.parametrize("B,H,Nq,Nkv,sb,sh,words", [
+    (4, 32, 4096, 4096, 0, 0, 16), (4, 32, 4096, 4096, 4, 0, 64), (4, 32, 4096, 4096, 0, 4, 512),
+    (4, 32, 4096, 4096, 8, 4, 2048), (1, 1, 1, 1, 0, 0, 1), (2, 3, 257, 4097, 0, 0, 4), (2, 3, 256, 4096, 4, 4, 6),
+    (1, 1, 0, 10, 0, 0, 0), (1, 1, 10, 0, 0, 0, 0), (0, 1, 10, 10, 0, 0, 0),
+])
+def test_mask_blocks_words(lib, B, H, Nq, Nkv, sb, sh, words):
+    """(sb ? B : 1) * (sh ? H : 1) * ceil(Nq / 256) * ceil(ceil(Nkv / 128) / 32)."""
+    assert lib.attn_mask_blocks_words(B, H, Nq, Nkv, sb, sh) == words
+
+
+def mask_blocks(lib, **kw):
+    a = dict(m=A, sb=0, sh=0, sq=4, B=1, H=1, Nq=16, Nkv=16, blocks=A2)
+    a.update(kw)
+    return lib.attn_mask_blocks(a["m"], a["sb"], a["sh"], a["sq"], a["B"], a["H"], a["Nq"], a["Nkv"], a["blocks"],
+                                None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(m=None), 1), (dict(m=ctypes.c_void_p(0x1004)), 1), (dict(sq=2), 1), (dict(sh=-4), 1),
+    (dict(blocks=None), 1), (dict(blocks=ctypes.c_void_p(0x2002)), 1), (dict(Nq=-1), 1), (dict(B=-1), 1),
+])
+def test_mask_blocks_rejects(lib, kw, expect):
+    assert mask_blocks(lib, **kw) == expect
+
+
+def masked_blocks(lib, **kw):
+    a = dict(q=A, k=A, v=A, o=A2, lse=None, B=2, H=2, N=16, D=64, causal=0, scale=0.125, dt=1,
+             m=A, sb=0, sh=0, sq=4, blocks=A2)
+    a.update(kw)
+    return lib.attn_fwd_masked_blocks(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                                      a["causal"], a["scale"], a["dt"], a["m"], a["sb"], a["sh"], a["sq"],
+                                      a["blocks"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(m=None), 1), (dict(m=ctypes.c_void_p(0x1004)), 1), (dict(sq=2), 1), (dict(blocks=None), 1),
+    (dict(blocks=ctypes.c_void_p(0x2002)), 1), (dict(q=None), 1), (dict(D=96), 2), (dict(dt=2), 2),
+    (dict(scale=-1.0), 1),
+])
+def test_attn_fwd_masked_blocks_rejects(lib, kw, expect):
+    assert masked_blocks(lib, **kw) == expect
 
 
 # --- split-K with the in-kernel merge ------------------------------------------------
