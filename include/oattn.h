@@ -25,9 +25,9 @@
  *     and the call returns without synchronising.  The attention kernels are launched
  *     as programmatic dependents of the previous kernel on the stream: they may be
  *     scheduled while it finishes and wait for its completion before touching memory.
- *     attn_fwd (key tiles of 128) launches one CTA per SM, each walking a share of the
- *     (head, query-tile pair) work; the masked, split-K and 32/64-key forms launch one
- *     CTA per query-tile pair.  Argument errors are returned before anything is
+ *     attn_fwd (key tiles of 128) and attn_fwd_masked_blocks launch one CTA per SM,
+ *     each walking a share of the (head, query-tile pair) work; attn_fwd_masked, the
+ *     split-K and the 32/64-key forms launch one CTA per query-tile pair.  Argument errors are returned before anything is
  *     launched; a failed launch returns OATTN_ERR_CUDA.
  *   - Scores are s = scale * q.k.  Causal masking keeps key index <= query index (the
  *     diagonal included) and requires equal query and key lengths.

@@ -878,12 +878,21 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     if (row0 < N) {
-      int tj = -1;  // key tile of iteration j (masked instances skip unmarked tiles)
+      // key tile of the next iteration (masked instances skip unmarked tiles) and, masked,
+      // this row's mask words for it: fetched one iteration ahead to hide the load
+      int tn = (MASK && skip) ? next_marked(s_need, 0) : 0;
+      uint4 wn = make_uint4(~0u, ~0u, ~0u, ~0u);
+      if constexpr (MASK) {
+        if (mrow != nullptr && nkv > 0) wn = ld_mask16(mrow + 4 * tn);
+      }
       for (int j = 0; j < nkv; ++j) {
-        tj = (MASK && skip) ? next_marked(s_need, tj + 1) : j;
-        uint4 w = make_uint4(~0u, ~0u, ~0u, ~0u);
-        if constexpr (MASK) {
-          if (mrow != nullptr) w = ld_mask16(mrow + 4 * tj);
+        const int tj = tn;
+        const uint4 w = wn;
+        if (j + 1 < nkv) {
+          tn = (MASK && skip) ? next_marked(s_need, tn + 1) : j + 1;
+          if constexpr (MASK) {
+            if (mrow != nullptr) wn = ld_mask16(mrow + 4 * tn);
+          }
         }
         ok = mbar_wait(&bar_s[t], (uint32_t)j & 1u, abort, status, kErrWaitS);
         ok = __all_sync(0xffffffffu, ok);
@@ -1340,11 +1349,18 @@ __global__ void __launch_bounds__(384, 1)
         }
         float m = -INFINITY;  // running max in use, log2 units of scale*s
         float l = 0.f;
-        int tj = -1;  // key tile of iteration j
+        // Masked: the key tile of the next iteration and this row's mask words for it are
+        // fetched one iteration ahead, so the load's latency hides behind a whole tile.
+        int tn = MASK ? next_marked(list, 0, mb.wpb) : 0;
+        uint4 wn = all_keys;
+        if (MASK && mrow != nullptr && nkv > 0) wn = ld_mask16(mrow + 4 * tn);
         for (int j = 0; j < nkv; ++j) {
-          tj = MASK ? next_marked(list, tj + 1, mb.wpb) : j;
-          uint4 w = all_keys;
-          if (MASK && mrow != nullptr) w = ld_mask16(mrow + 4 * tj);
+          const int tj = MASK ? tn : j;  // key tile of iteration j
+          const uint4 w = wn;
+          if (MASK && j + 1 < nkv) {
+            tn = next_marked(list, tn + 1, mb.wpb);
+            if (mrow != nullptr) wn = ld_mask16(mrow + 4 * tn);
+          }
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[t], (uint32_t)cs & 1u, abort, status, kErrWaitS));
           ++cs;
           if (!ok) break;
