@@ -168,6 +168,19 @@ def test_blocks_many_units_per_cta(causal):
                  heads=[(0, 0), (1, 3), (2, 45), (3, 79)])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocks_two_summary_words(causal):
+    """N = 5000: 40 key tiles, two summary words per block, per-head masks (the head
+    stride of the summary counts whole blocks of two words).  Head 0's band leaves key
+    tile 31 hidden, so its walk jumps from word 0 to word 1."""
+    B, Hh, N, D = 1, 2, 5000, 64
+    qb, kb, vb = H.qkv_host(470, B, Hh, N, D, "bf16")
+    m0 = synth.mask_band(N, N, 600)
+    m0[:, (np.arange(N) // 128) == 31] = False
+    mask = np.stack([m0, synth.mask_band(N, N, 1500)])[None]
+    check_blocks(qb, kb, vb, "bf16", mask, causal, f"blocks two words c{causal}")
+
+
 def test_blocks_all_visible_is_bitwise_unmasked():
     for causal in (False, True):
         qb, kb, vb = H.qkv_host(450, 2, 2, 700, 128, "bf16")
