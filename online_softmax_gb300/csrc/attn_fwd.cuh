@@ -1063,10 +1063,6 @@ __device__ __forceinline__ bool unit_item(int u, int s, int BH, int N, int causa
   return true;
 }
 
-// Masked form (MASK): the block summary of the mask (one bit per block of 256 query rows
-// and key tile) gives each item the key tiles it visits: marked tiles within its reach,
-// counted and walked alike by every role.  A query tile whose tiles are all unmarked
-// writes o = +0 and lse = -inf for its rows.
 // Item s of the i-th unit of this CTA: its summary words at list + (2 i + s) * wpb (zeros
 // where the unit has no such item).  Not inlined, so that none of its values stays live
 // into the roles (each role re-derives what it needs after setmaxnreg).
@@ -1090,6 +1086,10 @@ __device__ __noinline__ void fill_item_list(uint32_t* list, int BH, int N, int c
   }
 }
 
+// Masked form (MASK): the block summary of the mask (one bit per block of 256 query rows
+// and key tile) gives each item the key tiles it visits: marked tiles within its reach,
+// counted and walked alike by every role.  A query tile whose tiles are all unmarked
+// writes o = +0 and lse = -inf for its rows.
 template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
